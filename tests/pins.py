@@ -1,0 +1,393 @@
+"""Checks that pin the fp64 oracle to facts fixed outside itself.
+
+Each ``check_*`` takes the oracle function(s) under test as arguments, so the
+same check runs against the real oracle (tests/test_oracle_pins.py) and
+against deliberately broken copies of it (tests/test_oracle_mutations.py),
+which shows that a plausible mistake in the oracle fails at least one pin.
+
+What the pins rest on (never on the oracle itself):
+
+* the worked 16 x 16 mask of Fig. 2 (L=8, B=4), written out by hand in
+  tests/golden/ from the caption of "MARS: Enabling Autoregressive Models
+  Multi-Token Generation" and the three cases listed after its Eq. 2;
+* an independent 0-indexed construction of the mask from the blocks, as the
+  authors' blog post ("The construction, and the part that turned out to
+  matter") describes it in words;
+* the ratios the paper prints under Eq. 4 (25%, 12.5%, 6.25% for B = 4, 8, 16)
+  and the Sec. 3.3 statement that in-block position t sees t-1 placeholders;
+* textbook / library routines on special cases: torch's
+  scaled_dot_product_attention (causal) for the clean half and for each
+  noisy block, scipy's softmax / logsumexp, numpy's argmax;
+* closed forms: one visible key gives that key's value; equal keys give the
+  mean of the visible values; a one-hot logit row of height a has top-1
+  probability 1 / (1 + (V-1) e^-a);
+* the acceptance rules of the blog post ("Inference: a knob, not a mode
+  switch"): stop at the first position below tau, tau = 1.0 is plain AR, and
+  (aitrends.kr summary) at least one token is always committed.
+"""
+
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------------
+# helpers independent of the oracle
+# --------------------------------------------------------------------------
+
+def load_golden_mask(name="fig2_mask_L8_B4.txt"):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append([c == "1" for c in line])
+    return np.array(rows, dtype=bool)
+
+
+def blocks_of(L, B):
+    """0-indexed blocks of one stream: [start, stop) pairs; the last may be short."""
+    return [(s, min(s + B, L)) for s in range(0, L, B)]
+
+
+def mask_from_blocks(L, B):
+    """Visibility built from the blocks in words, 0-indexed, without Eq. 2's ceil().
+
+    The clean half is causal; a placeholder of noisy block k sees every clean
+    token before the start of block k and the placeholders of its own block
+    up to itself.
+    """
+    m = np.zeros((2 * L, 2 * L), dtype=bool)
+    for i in range(L):
+        m[i, : i + 1] = True
+    for start, stop in blocks_of(L, B):
+        for t in range(start, stop):
+            m[L + t, :start] = True
+            m[L + t, L + start: L + t + 1] = True
+    return m
+
+
+def sdpa_causal(q, k, v, scale):
+    """torch's causal scaled-dot-product attention in float64 (one head).
+
+    q: [n, D]; k, v: [n, D].  Query r sees keys 0..r.
+    """
+    import torch
+
+    tq = torch.from_numpy(np.ascontiguousarray(q))[None, None]
+    tk = torch.from_numpy(np.ascontiguousarray(k))[None, None]
+    tv = torch.from_numpy(np.ascontiguousarray(v))[None, None]
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=scale)
+    return out[0, 0].numpy()
+
+
+def rand(shape, seed, sigma=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * sigma
+
+
+# --------------------------------------------------------------------------
+# mask pins
+# --------------------------------------------------------------------------
+
+def check_mask_golden(mars_mask):
+    got = mars_mask(8, 4)
+    want = load_golden_mask()
+    assert got.shape == (16, 16)
+    assert np.array_equal(got, want), "Eq. 2 mask differs from the hand-written Fig. 2 mask"
+
+
+def check_mask_vs_blocks(mars_mask, Ls=(1, 2, 3, 5, 8, 10, 13, 16, 33), Bs=(1, 2, 3, 4, 5, 8, 16)):
+    for L in Ls:
+        for B in Bs:
+            assert np.array_equal(mars_mask(L, B), mask_from_blocks(L, B)), (L, B)
+
+
+def check_mask_pair_count(mars_mask):
+    for L, B in [(64, 4), (37, 5), (16, 16), (20, 32)]:
+        assert int(mars_mask(L, B).sum()) == L * (L + 1), (L, B)
+
+
+def check_mask_not_bidirectional(mars_mask):
+    """Block Diffusion's intra-block bidirectional mask is the contrast case (Fig. 2 caption)."""
+    L, B = 8, 4
+    m = mars_mask(L, B)
+    for start, stop in blocks_of(L, B):
+        for t in range(start, stop):
+            for u in range(t + 1, stop):
+                assert not m[L + t, L + u], "a placeholder sees a later placeholder"
+
+
+def check_mask_eq4_ratio(mars_mask):
+    """Eq. 4: the fraction of noisy positions with fully clean context is 1/B,
+    printed as 25%, 12.5%, 6.25% for B = 4, 8, 16."""
+    L = 64
+    for B, printed in [(4, 0.25), (8, 0.125), (16, 0.0625)]:
+        m = mars_mask(L, B)
+        noisy_keys_seen = m[L:, L:].sum(axis=1)
+        frac = np.mean(noisy_keys_seen == 1)
+        assert frac == printed, (B, frac)
+
+
+def check_mask_sec33_counts(mars_mask):
+    """Sec. 3.3: in-block position t (1-indexed) sees t-1 placeholders besides
+    itself plus the clean prefix of the earlier blocks."""
+    L, B = 24, 8
+    m = mars_mask(L, B)
+    for k, (start, stop) in enumerate(blocks_of(L, B)):
+        for t in range(start, stop):
+            t1 = t - start + 1
+            row = m[L + t]
+            assert row[L:].sum() == t1
+            assert row[:L].sum() == k * B
+            assert row[: k * B].all()
+
+
+# --------------------------------------------------------------------------
+# training attention pins
+# --------------------------------------------------------------------------
+
+def check_train_clean_half_is_causal(train_attn):
+    L, B, D = 24, 4, 16
+    q, k, v = rand((1, 2 * L, 1, D), 1), rand((1, 2 * L, 1, D), 2), rand((1, 2 * L, 1, D), 3)
+    scale = D ** -0.5
+    o, _ = train_attn(q, k, v, L, B, scale)
+    want = sdpa_causal(q[0, :L, 0], k[0, :L, 0], v[0, :L, 0], scale)
+    assert np.max(np.abs(o[0, :L, 0] - want)) < 1e-12
+
+
+def check_train_noisy_blocks_are_prefix_causal(train_attn, L=22, B=4, D=16):
+    """Each noisy block equals causal attention over [clean tokens of earlier
+    blocks ; that block's placeholders] (taking the block's rows)."""
+    q, k, v = rand((1, 2 * L, 1, D), 4), rand((1, 2 * L, 1, D), 5), rand((1, 2 * L, 1, D), 6)
+    scale = D ** -0.5
+    o, _ = train_attn(q, k, v, L, B, scale)
+    for start, stop in blocks_of(L, B):
+        idx = list(range(start)) + [L + t for t in range(start, stop)]
+        ref = sdpa_causal(q[0, idx, 0], k[0, idx, 0], v[0, idx, 0], scale)
+        got = o[0, L + start: L + stop, 0]
+        assert np.max(np.abs(got - ref[start:])) < 1e-12, (start, stop)
+
+
+def check_train_single_key_rows(train_attn):
+    """Clean position 0 and the first placeholder of block 1 see one key: out = v."""
+    L, B, D = 12, 4, 8
+    q, k, v = rand((2, 2 * L, 2, D), 7), rand((2, 2 * L, 1, D), 8), rand((2, 2 * L, 1, D), 9)
+    o, _ = train_attn(q, k, v, L, B, 0.3)
+    for b in range(2):
+        for h in range(2):
+            assert np.array_equal(o[b, 0, h], v[b, 0, 0])
+            assert np.array_equal(o[b, L, h], v[b, L, 0])
+
+
+def check_train_equal_keys_give_mean(train_attn):
+    L, B, D = 14, 3, 8
+    q = rand((1, 2 * L, 1, D), 10)
+    k = np.tile(rand((1, 1, 1, D), 11), (1, 2 * L, 1, 1))
+    v = rand((1, 2 * L, 1, D), 12)
+    o, _ = train_attn(q, k, v, L, B, 0.5)
+    vis = mask_from_blocks(L, B)
+    for i in range(2 * L):
+        want = v[0, vis[i], 0].mean(axis=0)
+        assert np.max(np.abs(o[0, i, 0] - want)) < 1e-12
+
+
+def check_train_bruteforce(train_attn):
+    """Naive triple loop, no max subtraction, on tiny shapes (small scale keeps exp finite)."""
+    L, B, D = 7, 3, 4
+    q, k, v = rand((1, 2 * L, 2, D), 13), rand((1, 2 * L, 1, D), 14), rand((1, 2 * L, 1, D), 15)
+    scale = 0.37
+    vis = mask_from_blocks(L, B)
+    o, lse = train_attn(q, k, v, L, B, scale)
+    for h in range(2):
+        for i in range(2 * L):
+            num = np.zeros(D)
+            den = 0.0
+            for j in range(2 * L):
+                if vis[i, j]:
+                    w = np.exp(scale * sum(q[0, i, h, d] * k[0, j, 0, d] for d in range(D)))
+                    num += w * v[0, j, 0]
+                    den += w
+            assert np.max(np.abs(o[0, i, h] - num / den)) < 1e-12
+            assert abs(lse[0, h, i] - np.log(den)) < 1e-12
+
+
+def check_train_lse(train_attn):
+    from scipy.special import logsumexp
+
+    L, B, D = 10, 4, 8
+    q, k, v = rand((1, 2 * L, 1, D), 16), rand((1, 2 * L, 1, D), 17), rand((1, 2 * L, 1, D), 18)
+    scale = D ** -0.5
+    _, lse = train_attn(q, k, v, L, B, scale)
+    vis = mask_from_blocks(L, B)
+    s = scale * q[0, :, 0] @ k[0, :, 0].T
+    for i in range(2 * L):
+        assert abs(lse[0, 0, i] - logsumexp(s[i, vis[i]])) < 1e-12
+
+
+def check_train_block_ge_L(train_attn):
+    """B >= L: one noisy block, so placeholders see no clean token at all."""
+    L, B, D = 9, 16, 8
+    q, k, v = rand((1, 2 * L, 1, D), 19), rand((1, 2 * L, 1, D), 20), rand((1, 2 * L, 1, D), 21)
+    scale = D ** -0.5
+    o, _ = train_attn(q, k, v, L, B, scale)
+    ref = sdpa_causal(q[0, L:, 0], k[0, L:, 0], v[0, L:, 0], scale)
+    assert np.max(np.abs(o[0, L:, 0] - ref)) < 1e-12
+
+
+def check_train_gqa_is_repeat_kv(train_attn):
+    """Query head h uses KV head h // (Hq/Hkv): same as repeating each KV head
+    Hq/Hkv times in a row (the Hugging Face repeat_kv layout)."""
+    L, B, D, hq, hkv = 10, 4, 8, 6, 2
+    q, k, v = rand((2, 2 * L, hq, D), 22), rand((2, 2 * L, hkv, D), 23), rand((2, 2 * L, hkv, D), 24)
+    o1, l1 = train_attn(q, k, v, L, B, 0.3)
+    o2, l2 = train_attn(q, np.repeat(k, hq // hkv, axis=2), np.repeat(v, hq // hkv, axis=2), L, B, 0.3)
+    assert np.max(np.abs(o1 - o2)) < 1e-13 and np.max(np.abs(l1 - l2)) < 1e-13
+    # and a hand-picked head: head 4 of 6 with 2 KV heads must read KV head 1
+    o3, _ = train_attn(q[:, :, 4:5], k[:, :, 1:2], v[:, :, 1:2], L, B, 0.3)
+    assert np.max(np.abs(o1[:, :, 4] - o3[:, :, 0])) < 1e-13
+
+
+def check_train_rows_subset(train_attn):
+    L, B, D = 12, 4, 8
+    q, k, v = rand((1, 2 * L, 2, D), 25), rand((1, 2 * L, 1, D), 26), rand((1, 2 * L, 1, D), 27)
+    o, lse = train_attn(q, k, v, L, B, 0.4)
+    rows = np.array([0, 5, 11, 12, 19, 23])
+    o2, lse2 = train_attn(q, k, v, L, B, 0.4, rows=rows)
+    assert np.max(np.abs(o[:, rows] - o2)) < 1e-13
+    assert np.max(np.abs(lse[:, :, rows] - lse2)) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# decode attention pins
+# --------------------------------------------------------------------------
+
+def check_decode_matches_train_block(decode_attn, train_attn):
+    """A decode step over cache = clean K/V of blocks < k and new = placeholders
+    of block k reproduces noisy block k of the training forward."""
+    L, B, D, hq, hkv = 20, 4, 8, 4, 2
+    q, k, v = rand((1, 2 * L, hq, D), 28), rand((1, 2 * L, hkv, D), 29), rand((1, 2 * L, hkv, D), 30)
+    scale = D ** -0.5
+    o_train, _ = train_attn(q, k, v, L, B, scale)
+    cap = L
+    for kb in range(L // B):
+        n = kb * B
+        kc = np.zeros((1, hkv, cap, D))
+        vc = np.zeros((1, hkv, cap, D))
+        kc[0, :, :n] = k[0, :n].transpose(1, 0, 2)
+        vc[0, :, :n] = v[0, :n].transpose(1, 0, 2)
+        rows = slice(L + n, L + n + B)
+        o = decode_attn(q[:, rows], k[:, rows], v[:, rows], kc, vc, np.array([n]), scale)
+        assert np.max(np.abs(o - o_train[:, rows])) < 1e-12, kb
+
+
+def check_decode_empty_cache_is_causal(decode_attn):
+    B, D = 6, 8
+    q, kn, vn = rand((1, B, 1, D), 31), rand((1, B, 1, D), 32), rand((1, B, 1, D), 33)
+    kc = np.zeros((1, 1, 4, D))
+    o = decode_attn(q, kn, vn, kc, kc, np.array([0]), 0.5)
+    ref = sdpa_causal(q[0, :, 0], kn[0, :, 0], vn[0, :, 0], 0.5)
+    assert np.max(np.abs(o[0, :, 0] - ref)) < 1e-12
+
+
+def check_decode_bruteforce(decode_attn):
+    """Per-sequence varlen cache, GQA, loop form."""
+    nb, B, D, hq, hkv, cap = 3, 3, 4, 4, 2, 9
+    q = rand((nb, B, hq, D), 34)
+    kn, vn = rand((nb, B, hkv, D), 35), rand((nb, B, hkv, D), 36)
+    kc, vc = rand((nb, hkv, cap, D), 37), rand((nb, hkv, cap, D), 38)
+    lens = np.array([0, 5, 9])
+    scale = 0.6
+    o = decode_attn(q, kn, vn, kc, vc, lens, scale)
+    for b in range(nb):
+        for h in range(hq):
+            g = h // (hq // hkv)
+            for i in range(B):
+                keys = [kc[b, g, j] for j in range(lens[b])] + [kn[b, c, g] for c in range(i + 1)]
+                vals = [vc[b, g, j] for j in range(lens[b])] + [vn[b, c, g] for c in range(i + 1)]
+                w = np.array([np.exp(scale * np.dot(q[b, i, h], kk)) for kk in keys])
+                want = (w[:, None] * np.array(vals)).sum(axis=0) / w.sum()
+                assert np.max(np.abs(o[b, i, h] - want)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# acceptance pins
+# --------------------------------------------------------------------------
+
+def check_accept_one_hot_closed_form(accept_rows):
+    V = 1000
+    for a, j in [(8.0, 17), (3.0, 999), (0.5, 0), (30.0, 512)]:
+        row = np.zeros(V)
+        row[j] = a
+        tok, conf = accept_rows(row[None, None, :])
+        assert tok[0, 0] == j
+        assert abs(conf[0, 0] - 1.0 / (1.0 + (V - 1) * np.exp(-a))) < 1e-13  # V-term fp64 sum
+
+
+def check_accept_ties_lowest_index(accept_rows):
+    row = np.zeros((1, 1, 50))
+    tok, conf = accept_rows(row)
+    assert tok[0, 0] == 0 and abs(conf[0, 0] - 1 / 50) < 1e-16
+    row[0, 0, [7, 31, 44]] = 2.5
+    tok, _ = accept_rows(row)
+    assert tok[0, 0] == 7
+    row[0, 0, 3] = -1.0
+    row[0, 0, 44] = 2.5
+    tok, _ = accept_rows(row)
+    assert tok[0, 0] == 7
+
+
+def check_accept_vs_library(accept_rows):
+    from scipy.special import softmax
+
+    x = rand((3, 5, 777), 39, sigma=3.0)
+    x = np.round(x * 4) / 4  # coarse grid: ties at the max happen
+    tok, conf = accept_rows(x)
+    for b in range(3):
+        for i in range(5):
+            assert tok[b, i] == int(np.argmax(x[b, i]))
+            assert abs(conf[b, i] - softmax(x[b, i]).max()) < 1e-12
+
+
+def check_commit_rule(commit_count):
+    assert commit_count([0.5, 0.99, 0.99, 0.99], 0.9) == 1      # first below tau: still one token
+    assert commit_count([0.99, 0.99, 0.5, 0.99], 0.9) == 2      # stop at the first below tau
+    assert commit_count([0.99, 0.95, 0.96, 0.999], 0.95) == 4   # conf == tau passes
+    assert commit_count([0.2, 0.3, 0.1], 0.0) == 3              # tau = 0 commits all B
+    assert commit_count([0.999999, 0.9999999], 1.0) == 1        # tau = 1.0 is plain AR
+    assert commit_count([0.3, 0.95, 0.97, 0.2], 0.9) == 1       # confident later positions never count
+    assert commit_count([0.91], 0.9) == 1
+
+
+def check_accept_tau_extremes(accept):
+    x = rand((4, 6, 300), 40, sigma=2.0)
+    x[1, :, 5] += 20.0
+    tok, conf, n = accept(x, 1.0)
+    assert np.all(n == 1)
+    tok, conf, n = accept(x, float(conf.max()) + 1e-9)
+    assert np.all(n == 1)
+    tok, conf, n = accept(x, 0.0)
+    assert np.all(n == 6)
+
+
+def check_append(append_kv):
+    nb, B, hkv, D, cap = 3, 4, 2, 5, 12
+    kc, vc = rand((nb, hkv, cap, D), 41), rand((nb, hkv, cap, D), 42)
+    kn, vn = rand((nb, B, hkv, D), 43), rand((nb, B, hkv, D), 44)
+    lens = np.array([0, 3, 8])
+    n = np.array([1, 4, 2])
+    kc2, vc2, lens2 = append_kv(kc, vc, lens, kn, vn, n)
+    assert np.array_equal(lens2, lens + n)
+    for b in range(nb):
+        for g in range(hkv):
+            for p in range(cap):
+                if lens[b] <= p < lens[b] + n[b]:
+                    assert np.array_equal(kc2[b, g, p], kn[b, p - lens[b], g])
+                    assert np.array_equal(vc2[b, g, p], vn[b, p - lens[b], g])
+                else:
+                    assert np.array_equal(kc2[b, g, p], kc[b, g, p])
+                    assert np.array_equal(vc2[b, g, p], vc[b, g, p])
