@@ -1,0 +1,145 @@
+/*
+ * mars.h - C ABI of libmars, the GB300 (sm_103a) hot path of MARS
+ * (Mask AutoRegreSsion) multi-token generation.
+ *
+ * Method sources, cited by page title and section / equation:
+ *   [paper] "MARS: Enabling Autoregressive Models Multi-Token Generation"
+ *           (arXiv 2604.07023).
+ *   [blog]  the authors' MARS blog post (xalp.net/posts/2026-06-mars).
+ *   [news]  "MARS: 자기회귀 모델의 멀티 토큰 생성을 가능하게 하는 기법" (aitrends.kr).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are caller-owned DEVICE pointers, dense row-major in the shapes
+ *   written beside each argument.  bf16 values are passed as their 16-bit
+ *   patterns (uint16_t), i.e. the storage of __nv_bfloat16 / torch.bfloat16.
+ * - Every tensor pointer must be 16-byte aligned.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and never allocate, free or synchronise.  They can be captured in a
+ *   CUDA graph.
+ * - The return value reports what the host can see before launch; conditions
+ *   that only the device can see are OR-ed into the optional device status
+ *   word (`int32_t*` in device memory, may be NULL), which the caller reads
+ *   after the stream has completed and clears when it wants to.
+ * - Inputs must be finite.  The result for NaN / Inf inputs is unspecified
+ *   (no fault: it is only arithmetic on the values).
+ * - GQA: query head h reads KV head h / (Hq / Hkv) (contiguous groups).
+ */
+#ifndef MARS_H_
+#define MARS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-visible return codes. */
+#define MARS_OK 0
+#define MARS_ERR_INVALID_ARG 1         /* null / misaligned pointer, bad size, unsupported shape */
+#define MARS_ERR_WORKSPACE_TOO_SMALL 2 /* workspace smaller than the *_workspace_size() answer */
+#define MARS_ERR_CUDA 3                /* a CUDA runtime call or a launch failed */
+#define MARS_ERR_UNSUPPORTED_DEVICE 4  /* current device is not compute capability 10.3 */
+
+/* Bits that kernels OR into the device status word. */
+#define MARS_DEV_CAPACITY 1   /* mars_accept: cache_len + n_commit would exceed cap; that sequence was not appended */
+#define MARS_DEV_LEN_RANGE 2  /* mars_decode_attn: a cache_len[b] was < 0 or > max_len; that sequence's output is zero */
+#define MARS_DEV_TIMEOUT 4    /* mars_train_attn: an internal pipeline wait hit its iteration limit; output incomplete */
+
+/* Human-readable text for a return code (static storage, never NULL). */
+const char* mars_status_string(int status);
+
+/* Library ABI version: 100 * major + minor. */
+int mars_version(void);
+
+/*
+ * mars_train_attn - attention over the concatenated sequence z = [x ; x~]
+ * under the MARS structured mask ([paper] Sec. 3.2, Eq. 1 and Eq. 2).
+ *
+ * Positions 0..L-1 of z are the clean stream, L..2L-1 the noisy ([MASK])
+ * stream.  With 0-indexed query i and key j:
+ *   clean query (i < L):       sees clean keys j <= i                    (causal)
+ *   noisy query i = L + t:     sees clean keys j < B * floor(t / B)       (earlier blocks)
+ *                              and noisy keys L + u with floor(u / B) == floor(t / B), u <= t
+ * L need not be a multiple of B (the last block is short).
+ *
+ *   q    [batch, 2L, Hq,  D]  bf16          o   [batch, 2L, Hq, D] bf16 (written)
+ *   k, v [batch, 2L, Hkv, D]  bf16          lse [batch, Hq, 2L] fp32, natural-log
+ *                                               log-sum-exp of the scaled masked
+ *                                               scores (may be NULL)
+ *   scale: multiplies q.k (normally 1/sqrt(D)).
+ * Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= B; 1 <= L <= 65536.
+ * Fully masked tiles are skipped; no workspace.
+ */
+int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    uint16_t* o, float* lse,
+                    int batch, int L, int B, int Hq, int Hkv, int D, float scale,
+                    int32_t* status, void* stream);
+
+/*
+ * mars_decode_attn - attention of one sliding-window decode step
+ * ([paper] Fig. 2 right: B [MASK] tokens appended after the cursor and
+ * filled by one forward; [blog] "Inference: a knob, not a mode switch").
+ *
+ * Query i (0 <= i < B) of sequence b sees the cache_len[b] committed keys of
+ * its KV head and the new keys c <= i of this step (causal among the
+ * placeholders, as in the noisy intra-block case of Eq. 2).
+ *
+ *   q              [batch, B, Hq, D]     bf16
+ *   k_new, v_new   [batch, B, Hkv, D]    bf16  (K/V of this step's B positions)
+ *   k_cache, v_cache [batch, Hkv, cap, D] bf16 (block-level KV cache, read only)
+ *   cache_len      [batch] int32, device; every value in [0, max_len]
+ *   o              [batch, B, Hq, D]     bf16 (written)
+ * Supported: D in {64, 128}; 1 <= B <= 16; Hq % Hkv == 0; max_len <= cap.
+ * A cache_len outside [0, max_len] sets MARS_DEV_LEN_RANGE and that
+ * sequence's output is written as zeros.  No workspace.
+ */
+int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                     const uint16_t* k_cache, const uint16_t* v_cache,
+                     const int32_t* cache_len,
+                     int batch, int B, int Hq, int Hkv, int D, int cap, int max_len,
+                     float scale, uint16_t* o, int32_t* status, void* stream);
+
+/*
+ * mars_accept - confidence-threshold acceptance with the block-level KV
+ * append ([blog] "Inference: a knob, not a mode switch": commit left to right
+ * while the top-1 probability holds, stop at the first position below tau;
+ * [paper] Sec. 3.1 gap (4): strictly left-to-right; [news]: at least one
+ * token is always accepted; [paper] contributions: block-level KV cache).
+ *
+ * For each row (b, i):  m = max_v logits, tokens = smallest v with logits == m,
+ *                       conf = 1 / sum_v exp(logits - m)   (top-1 probability)
+ * For each sequence b:  n = number of leading i with conf >= tau, then max(n, 1);
+ *                       rows 0..n-1 of k_new / v_new are copied to cache
+ *                       positions cache_len[b] .. cache_len[b]+n-1 and
+ *                       cache_len[b] += n.
+ *
+ *   logits           [batch, B, V] bf16
+ *   k_new, v_new     [batch, B, Hkv, D] bf16
+ *   k_cache, v_cache [batch, Hkv, cap, D] bf16 (updated in place)
+ *   cache_len        [batch] int32, device, in/out
+ *   tokens [batch, B] int32, conf [batch, B] fp32, n_commit [batch] int32 (written)
+ *   workspace        device buffer of >= mars_accept_workspace_size(batch, B, V)
+ *                    bytes, zero-filled before its first use.  It holds per-slice
+ *                    partial results and completion counters; every call returns
+ *                    the counters to zero, so the same buffer is passed unchanged
+ *                    to the next call.  Calls that share a workspace must not
+ *                    overlap in time.
+ * If cache_len[b] + n > cap nothing is appended for b, cache_len[b] is kept,
+ * n_commit[b] is 0 and MARS_DEV_CAPACITY is set.
+ * Supported: 1 <= B <= 16, 1 <= V, D % 8 == 0, D <= 256.
+ */
+size_t mars_accept_workspace_size(int batch, int B, int V);
+int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau,
+                const uint16_t* k_new, const uint16_t* v_new,
+                uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
+                int Hkv, int D, int cap,
+                int32_t* tokens, float* conf, int32_t* n_commit,
+                int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MARS_H_ */

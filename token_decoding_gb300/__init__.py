@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) hot path of MARS multi-token generation.
+
+The compute lives in libmars.so (hand-written CUDA, C ABI in include/mars.h);
+this package only marshals arguments (``_lib``), builds the library
+(``build``) and draws seeded synthetic inputs (``synth``).
+"""
+from ._lib import (  # noqa: F401
+    MARS_DEV_CAPACITY,
+    MARS_DEV_LEN_RANGE,
+    MARS_DEV_TIMEOUT,
+    MarsError,
+    accept,
+    accept_workspace,
+    accept_workspace_size,
+    decode_attn,
+    lib,
+    status_string,
+    train_attn,
+    version,
+)

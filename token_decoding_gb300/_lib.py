@@ -1,0 +1,214 @@
+"""ctypes binding of libmars (argument marshalling only).
+
+Every function here checks tensor shapes / dtypes / devices, then calls the
+C entry point of the same name with raw device pointers and the current CUDA
+stream.  All computation happens in the CUDA kernels of libmars.so; there is
+no fallback of any kind: if the library is not built, or a call fails, a
+RuntimeError is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmars.so")
+
+MARS_OK = 0
+MARS_ERR_INVALID_ARG = 1
+MARS_ERR_WORKSPACE_TOO_SMALL = 2
+MARS_ERR_CUDA = 3
+MARS_ERR_UNSUPPORTED_DEVICE = 4
+
+MARS_DEV_CAPACITY = 1
+MARS_DEV_LEN_RANGE = 2
+MARS_DEV_TIMEOUT = 4
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "mars_status_string": (ctypes.c_char_p, [_I]),
+    "mars_version": (_I, []),
+    "mars_train_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
+    "mars_accept": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+}
+
+_lib = None
+
+
+class MarsError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmars.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m token_decoding_gb300.build` "
+                "(or __graft_entry__.build()); there is no fallback path")
+        _lib = ctypes.CDLL(LIB_PATH)
+    return _lib
+
+
+_fns = {}
+
+
+def _fn(name):
+    """The C entry point `name` with its ctypes signature (resolved on first use)."""
+    f = _fns.get(name)
+    if f is None:
+        f = getattr(lib(), name)
+        res, args = _SIGNATURES[name]
+        f.restype = res
+        f.argtypes = args
+        _fns[name] = f
+    return f
+
+
+def status_string(code: int) -> str:
+    return _fn("mars_status_string")(int(code)).decode()
+
+
+def version() -> int:
+    return int(_fn("mars_version")())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, shape, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _call(name, *args):
+    rc = _fn(name)(*args)
+    if rc != MARS_OK:
+        raise MarsError(name, rc)
+
+
+def train_attn(q, k, v, L: int, B: int, scale: float | None = None, o=None, lse=None, status=None,
+               want_lse: bool = False, stream=None):
+    """MARS masked attention over z = [x ; x~] (see include/mars.h: mars_train_attn).
+
+    q [b, 2L, Hq, D], k/v [b, 2L, Hkv, D] bf16 CUDA tensors.  Returns o (and lse
+    when ``want_lse`` or ``lse`` is given).
+    """
+    nb, n2, hq, d = q.shape
+    hkv = k.shape[2]
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (nb, 2 * L, hq, d))
+    _check(k, "k", torch.bfloat16, (nb, 2 * L, hkv, d), dev)
+    _check(v, "v", torch.bfloat16, (nb, 2 * L, hkv, d), dev)
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", torch.bfloat16, q.shape, dev)
+    if lse is None and want_lse:
+        lse = torch.empty((nb, hq, 2 * L), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (nb, hq, 2 * L), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_train_attn", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), nb, L, B, hq, hkv, d, float(scale),
+          _ptr(status), _stream(stream))
+    return (o, lse) if lse is not None else o
+
+
+def decode_attn(q, k_new, v_new, k_cache, v_cache, cache_len, max_len: int, scale: float | None = None, o=None,
+                status=None, stream=None):
+    """Attention of one sliding-window decode step (include/mars.h: mars_decode_attn)."""
+    nb, bq, hq, d = q.shape
+    hkv = k_new.shape[2]
+    cap = k_cache.shape[2]
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (nb, bq, hq, d))
+    _check(k_new, "k_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(v_new, "v_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(k_cache, "k_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(cache_len, "cache_len", torch.int32, (nb,), dev)
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", torch.bfloat16, q.shape, dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_decode_attn", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
+          nb, bq, hq, hkv, d, cap, int(max_len), float(scale), _ptr(o), _ptr(status), _stream(stream))
+    return o
+
+
+def accept_workspace_size(batch: int, B: int, V: int) -> int:
+    return int(_fn("mars_accept_workspace_size")(batch, B, V))
+
+
+def accept_workspace(batch: int, B: int, V: int, device) -> torch.Tensor:
+    """A zero-filled workspace for accept (its counters return to zero after every call)."""
+    n = accept_workspace_size(batch, B, V)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, workspace=None, tokens=None, conf=None,
+           n_commit=None, status=None, stream=None):
+    """Greedy tokens, top-1 probabilities, left-to-right commit and KV append
+    (include/mars.h: mars_accept).  Returns (tokens, conf, n_commit); k_cache,
+    v_cache and cache_len are updated in place."""
+    nb, bq, V = logits.shape
+    hkv, d = k_new.shape[2], k_new.shape[3]
+    cap = k_cache.shape[2]
+    dev = logits.device
+    _check(logits, "logits", torch.bfloat16, (nb, bq, V))
+    _check(k_new, "k_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(v_new, "v_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(k_cache, "k_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(cache_len, "cache_len", torch.int32, (nb,), dev)
+    if workspace is None:
+        workspace = accept_workspace(nb, bq, V, dev)
+    if tokens is None:
+        tokens = torch.empty((nb, bq), dtype=torch.int32, device=dev)
+    if conf is None:
+        conf = torch.empty((nb, bq), dtype=torch.float32, device=dev)
+    if n_commit is None:
+        n_commit = torch.empty((nb,), dtype=torch.int32, device=dev)
+    _check(tokens, "tokens", torch.int32, (nb, bq), dev)
+    _check(conf, "conf", torch.float32, (nb, bq), dev)
+    _check(n_commit, "n_commit", torch.int32, (nb,), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_accept", _ptr(logits), nb, bq, V, float(tau), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+          _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
+          _ptr(workspace), workspace.numel(), _stream(stream))
+    return tokens, conf, n_commit
