@@ -1,0 +1,612 @@
+"""Benchmark of the MARS hot path on GB300 (one JSON line on rank 0).
+
+One step runs every stage of the path on synthetic Qwen2.5-shaped inputs:
+  * mars_train_attn on the Qwen2.5-0.5B-shaped training batch (b4, L=1024,
+    B=4, 14/2 heads, D=64)                          -> headline value, TFLOP/s
+  * mars_train_attn on the Qwen2.5-7B-shaped batch (b2, L=2048, B=8, 28/4, D=128)
+  * one sliding-window decode step at batch 64 (varlen caches 256..4096, B=8,
+    28/4 heads, D=128, V=152064): mars_decode_attn then mars_accept (+ KV append)
+  * one decode step at batch 1 (cache 2048, B=4): decode attention + accept
+Every kernel is timed with CUDA events on the stream it runs on; inputs rotate
+over enough buffers that each kernel's working set exceeds twice the L2, so
+nothing is served from a warm L2 between iterations.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "train-mask attn TFLOP/s; decode attn+accept GB/s & steps/s; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 126 * 1024 * 1024
+DECODE_TAU = 0.95
+CONFIG = {
+    "workload": ("mars step: train-mask attn Qwen2.5-0.5B shape (b4 L1024 B4 14/2 d64; headline value) + "
+                 "train-mask attn Qwen2.5-7B shape (b2 L2048 B8 28/4 d128) + batched decode step "
+                 "(b64, cache 256..4096, B8, 28/4 d128, V152064: decode attn + accept/append, tau 0.95) + "
+                 "batch-1 decode step (cache 2048, B4, V152064)"),
+    "l2": "inputs rotate over buffer sets so each kernel's working set is >= 2x L2",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "token_decoding_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes from the committed ncu capture, if the kernels are unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if t.get("kernel_sources_sha") != kernel_sources_sha():
+        return {}
+    return t.get("traffic_bytes_per_launch", {})
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas only: the path has no exchange step)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, world):
+    if world > 1:
+        dist.barrier()
+
+
+def max_over_ranks(dist, world, value, device):
+    if world == 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, world, value, device):
+    if world == 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+
+        fd, self.path = tempfile.mkstemp(prefix="mars_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def roofline(bound, achieved, peak, unit, traffic):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic}
+
+
+def spiked_logits_gpu(batch, B, V, sigma, prob, lo, hi, gen, device):
+    import torch
+
+    x = torch.randn((batch, B, V), generator=gen, device=device, dtype=torch.float32) * sigma
+    spiked = torch.rand((batch, B), generator=gen, device=device) < prob
+    tok = torch.randint(0, V, (batch, B), generator=gen, device=device)
+    height = lo + (hi - lo) * torch.rand((batch, B), generator=gen, device=device)
+    x.scatter_add_(2, tok.unsqueeze(-1), (height * spiked).unsqueeze(-1))
+    return x.to(torch.bfloat16)
+
+
+class TrainWork:
+    def __init__(self, shape, device, gen, min_bytes):
+        import torch
+
+        s = shape
+        self.s = s
+        per = (2 * s.batch * 2 * s.L * (s.Hq + s.Hkv) * s.D) * 2   # q + o + k + v bytes
+        self.nsets = max(1, -(-min_bytes // per))
+        self.sets = []
+        for _ in range(self.nsets):
+            q = torch.randn((s.batch, 2 * s.L, s.Hq, s.D), generator=gen, device=device).to(torch.bfloat16)
+            k = torch.randn((s.batch, 2 * s.L, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+            v = torch.randn((s.batch, 2 * s.L, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+            self.sets.append((q, k, v, torch.empty_like(q)))
+        self.flops = s.useful_flops
+
+    def run(self, mars, step):
+        q, k, v, o = self.sets[step % self.nsets]
+        mars.train_attn(q, k, v, self.s.L, self.s.B, o=o)
+
+
+class DecodeWork:
+    """One sliding-window decode step (decode attention, then accept + append)."""
+
+    def __init__(self, shape, device, gen, min_bytes, steps_per_episode):
+        import torch
+        from token_decoding_gb300 import synth
+
+        import token_decoding_gb300 as mars
+
+        s = shape
+        self.s = s
+        lens0 = synth.initial_cache_lens(s)
+        self.lens0_host = lens0.astype(np.int64)
+        cache_bytes = int(lens0.sum()) * s.Hkv * s.D * 2 * 2
+        per = cache_bytes + s.batch * s.B * s.V * 2
+        self.nsets = max(1, -(-min_bytes // per))
+        self.sets = []
+        for _ in range(self.nsets):
+            kc = torch.randn((s.batch, s.Hkv, s.cap, s.D), generator=gen, device=device).to(torch.bfloat16)
+            vc = torch.randn((s.batch, s.Hkv, s.cap, s.D), generator=gen, device=device).to(torch.bfloat16)
+            lens = torch.from_numpy(lens0.copy()).to(device)
+            logits = spiked_logits_gpu(s.batch, s.B, s.V, s.base_sigma, s.spike_prob, s.spike_lo, s.spike_hi,
+                                       gen, device)
+            ws = mars.accept_workspace(s.batch, s.B, s.V, device)
+            self.sets.append({"kc": kc, "vc": vc, "lens": lens, "logits": logits, "ws": ws})
+        self.lens0 = torch.from_numpy(lens0.copy()).to(device)
+        self.q = torch.randn((s.batch, s.B, s.Hq, s.D), generator=gen, device=device).to(torch.bfloat16)
+        self.kn = torch.randn((s.batch, s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+        self.vn = torch.randn((s.batch, s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+        self.o = torch.empty_like(self.q)
+        self.tokens = torch.empty((s.batch, s.B), dtype=torch.int32, device=device)
+        self.conf = torch.empty((s.batch, s.B), dtype=torch.float32, device=device)
+        self.episode = steps_per_episode
+        self.max_len = s.cap - s.B
+
+    def reset(self):
+        """Start a new episode: every buffer set goes back to the initial cache lengths."""
+        for st in self.sets:
+            st["lens"].copy_(self.lens0)
+
+    def run_decode(self, mars, step):
+        st = self.sets[step % self.nsets]
+        mars.decode_attn(self.q, self.kn, self.vn, st["kc"], st["vc"], st["lens"], self.max_len, o=self.o)
+
+    def run_accept(self, mars, step, n_out):
+        st = self.sets[step % self.nsets]
+        mars.accept(st["logits"], DECODE_TAU, self.kn, self.vn, st["kc"], st["vc"], st["lens"], workspace=st["ws"],
+                    tokens=self.tokens, conf=self.conf, n_commit=n_out)
+
+    def byte_counts(self, records):
+        """Algorithmic bytes of decode and accept per executed step, from the commit history."""
+        s = self.s
+        lens = {i: self.lens0_host.copy() for i in range(self.nsets)}
+        dec, acc = [], []
+        small = s.batch * s.B * (2 * s.Hkv + 2 * s.Hq) * s.D * 2
+        for kind, set_idx, n in records:
+            if kind == "reset":
+                lens = {i: self.lens0_host.copy() for i in range(self.nsets)}
+                continue
+            L = lens[set_idx]
+            dec.append(int(L.sum()) * s.Hkv * s.D * 2 * 2 + small)
+            ncommit = n.astype(np.int64)
+            acc.append(s.batch * s.B * s.V * 2 + int(ncommit.sum()) * s.Hkv * s.D * 2 * 2 * 2
+                       + s.batch * s.B * 8 + s.batch * 8)
+            lens[set_idx] = L + ncommit
+        return dec, acc
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import token_decoding_gb300 as mars
+    from token_decoding_gb300 import build as mars_build
+    from token_decoding_gb300 import synth
+
+    if not os.path.exists(mars._lib.LIB_PATH):
+        mars_build.build()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    peaks, peak_src = load_peaks()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234 + rank)
+    min_bytes = 2 * L2_BYTES
+
+    train05 = TrainWork(synth.TRAIN_05B, device, gen, min_bytes)
+    train7 = TrainWork(synth.TRAIN_7B, device, gen, min_bytes)
+    dec64 = DecodeWork(synth.DECODE_7B_B64, device, gen, min_bytes, steps_per_episode=synth.DECODE_7B_B64.steps)
+    dec1 = DecodeWork(synth.DECODE_7B_B1, device, gen, min_bytes, steps_per_episode=synth.DECODE_7B_B1.steps)
+    total = args.warmup + args.steps
+    ncommit64 = torch.zeros((total, dec64.s.batch), dtype=torch.int32, device=device)
+    ncommit1 = torch.zeros((total, dec1.s.batch), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    names = ["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1", "accept_b1"]
+    records64, records1 = [], []
+
+    def step(i, ev):
+        if i % dec64.episode == 0:
+            dec64.reset()
+            records64.append(("reset", 0, None))
+        if i % dec1.episode == 0:
+            dec1.reset()
+            records1.append(("reset", 0, None))
+        if ev is not None:
+            ev[0].record(stream)
+        train05.run(mars, i)
+        if ev is not None:
+            ev[1].record(stream)
+        train7.run(mars, i)
+        if ev is not None:
+            ev[2].record(stream)
+        dec64.run_decode(mars, i)
+        if ev is not None:
+            ev[3].record(stream)
+        dec64.run_accept(mars, i, ncommit64[i])
+        records64.append(("step", i % dec64.nsets, i))
+        if ev is not None:
+            ev[4].record(stream)
+        dec1.run_decode(mars, i)
+        if ev is not None:
+            ev[5].record(stream)
+        dec1.run_accept(mars, i, ncommit1[i])
+        records1.append(("step", i % dec1.nsets, i))
+        if ev is not None:
+            ev[6].record(stream)
+
+    for i in range(args.warmup):
+        step(i, None)
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    barrier(dist, world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + k, events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(dist, world)
+    total_ms = t_start.elapsed_time(t_end)
+    per_kernel_ms = {n: [events[k][j].elapsed_time(events[k][j + 1]) for k in range(args.steps)]
+                     for j, n in enumerate(names)}
+    total_ms = max_over_ranks(dist, world, total_ms, device)
+
+    # algorithmic work of the timed steps
+    n64 = ncommit64.cpu().numpy()
+    n1 = ncommit1.cpu().numpy()
+
+    def resolve(records, hist):
+        out = []
+        for kind, set_idx, i in records:
+            out.append((kind, set_idx, None if kind == "reset" else hist[i]))
+        return out
+
+    dec64_b, acc64_b = dec64.byte_counts(resolve(records64, n64))
+    dec1_b, acc1_b = dec1.byte_counts(resolve(records1, n1))
+    timed = slice(args.warmup, args.warmup + args.steps)
+    work = {
+        "train_05b": ("tensor", [train05.flops] * args.steps, "TFLOP/s", 1e-12),
+        "train_7b": ("tensor", [train7.flops] * args.steps, "TFLOP/s", 1e-12),
+        "decode_attn_b64": ("hbm", dec64_b[timed], "GB/s", 1e-9),
+        "accept_b64": ("hbm", acc64_b[timed], "GB/s", 1e-9),
+        "decode_attn_b1": ("hbm", dec1_b[timed], "GB/s", 1e-9),
+        "accept_b1": ("hbm", acc1_b[timed], "GB/s", 1e-9),
+    }
+    traffic = ncu_traffic()
+    parts = {}
+    for n in names:
+        bound, units, unit, scale = work[n]
+        ms = sum(per_kernel_ms[n])
+        achieved = sum(units) * scale / (ms * 1e-3)
+        peak = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
+        parts[n] = {
+            "avg_us": round(ms / args.steps * 1e3, 3),
+            "roofline": roofline(bound, achieved, peak, unit, traffic.get(n)),
+        }
+        if bound == "tensor":
+            parts[n]["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+    for tag, dec_n, acc_n, shape in (("b64", "decode_attn_b64", "accept_b64", dec64.s),
+                                     ("b1", "decode_attn_b1", "accept_b1", dec1.s)):
+        ms = sum(per_kernel_ms[dec_n]) + sum(per_kernel_ms[acc_n])
+        byts = sum(work[dec_n][1]) + sum(work[acc_n][1])
+        parts[f"decode_step_{tag}"] = {
+            "steps_per_s": round(args.steps / (ms * 1e-3), 1),
+            "GB_per_s": round(byts / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "tokens_per_step": round(float(n64[timed].sum(axis=1).mean() if tag == "b64" else
+                                           n1[timed].sum(axis=1).mean()), 3),
+        }
+    dominant = max(names, key=lambda n: sum(per_kernel_ms[n]))
+
+    # headline: training-mask attention TFLOP/s on the Qwen2.5-0.5B-shaped batch
+    t05_ms = max_over_ranks(dist, world, sum(per_kernel_ms["train_05b"]), device)
+    value = sum_over_ranks(dist, world, train05.flops * args.steps, device) / (t05_ms * 1e-3) / 1e12
+
+    # end to end through the public API with pinned host buffers
+    e2e = run_e2e(args, mars, train05, device, stream, dist, world)
+    graph = None if args.no_graph else run_b1_graph(args, mars, dec1, device)
+    if graph is not None:
+        parts["decode_step_b1"]["graph_steps_per_s"] = graph
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v/caches, spiked N(0,1)*2 logits; Qwen2.5-0.5B/7B shapes)",
+        "config": dict(CONFIG, parallelism="replicas" if world > 1 else "single GPU", peaks=peak_src),
+        "roofline": parts[dominant]["roofline"],
+        "roofline_kernel": dominant,
+        "parts": parts,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": 6 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, mars, work, device, stream, dist, world):
+    """Headline metric end to end: pinned host inputs -> device -> kernel -> host."""
+    import torch
+
+    s = work.s
+    q, k, v, o = work.sets[0]
+    hq = [t.cpu().pin_memory() for t in (q, k, v)]
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    steps = max(1, args.steps)
+    for _ in range(2):
+        q.copy_(hq[0], non_blocking=True)
+        mars.train_attn(q, k, v, s.L, s.B, o=o)
+        ho.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(dist, world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        q.copy_(hq[0], non_blocking=True)
+        k.copy_(hq[1], non_blocking=True)
+        v.copy_(hq[2], non_blocking=True)
+        mars.train_attn(q, k, v, s.L, s.B, o=o)
+        ho.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(dist, world, e0.elapsed_time(e1), device)
+    h2d = sum(t.numel() * t.element_size() for t in hq)
+    d2h = ho.numel() * ho.element_size()
+    val = work.flops * steps * world / (ms * 1e-3) / 1e12
+    return {"value": round(val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_b1_graph(args, mars, work, device):
+    """Batch-1 decode loop (decode attention + accept) captured as one CUDA graph of 256 steps."""
+    import torch
+
+    n_steps = work.s.steps
+    stream = torch.cuda.Stream(device=device)
+    n_out = torch.zeros((n_steps, 1), dtype=torch.int32, device=device)
+    with torch.cuda.stream(stream):
+        work.reset()
+        for i in range(2):
+            work.run_decode(mars, i)
+            work.run_accept(mars, i, n_out[i])
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n_steps):
+                work.run_decode(mars, i)
+                work.run_accept(mars, i, n_out[i])
+        reps = 3
+        work.reset()
+        graph.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        ms = 0.0
+        for _ in range(reps):
+            work.reset()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            stream.synchronize()
+            ms += e0.elapsed_time(e1)
+    return round(reps * n_steps / (ms * 1e-3), 1)
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_train_sample(budget_s):
+    """Time the fp64 oracle on whole (batch, head) slices of the 0.5B-shaped
+    training batch until about budget_s seconds have passed; returns
+    (useful TFLOP/s, description, seconds)."""
+    import oracle
+    from token_decoding_gb300 import synth
+
+    s = synth.TRAIN_05B
+    q, k, v = synth.train_inputs(s)
+    per_head = 4 * s.D * s.L * (s.L + 1)
+    done = 0
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        b, h = divmod(heads % (s.batch * s.Hq), s.Hq)
+        g = h // (s.Hq // s.Hkv)
+        oracle.train_attn(q.f64[b:b + 1, :, h:h + 1], k.f64[b:b + 1, :, g:g + 1], v.f64[b:b + 1, :, g:g + 1],
+                          s.L, s.B, s.D ** -0.5)
+        done += per_head
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el / 1e12, f"{heads} (batch, head) slices of {s.name}, fp64 numpy, dense 2L x 2L masked", el
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s):
+    val, sample, _ = oracle_train_sample(budget_s)
+    return {"value": round(val, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": sample + " (numpy BLAS threads: all available cores)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    budget = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_train_sample(budget)
+    vals, secs = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        v, desc, el = oracle_train_sample(budget)
+        vals.append(v)
+        secs += el
+    value = float(np.mean(vals)) if vals else 0.0
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(CONFIG, parallelism="single process on the host cores"),
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["mars", "reference"], default="mars")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph batch-1 decode loop")
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -13,7 +13,9 @@
  * - Tensors are caller-owned DEVICE pointers, dense row-major in the shapes
  *   written beside each argument.  bf16 values are passed as their 16-bit
  *   patterns (uint16_t), i.e. the storage of __nv_bfloat16 / torch.bfloat16.
- * - Every tensor pointer must be 16-byte aligned.
+ * - Alignment: bf16 tensors must be 16-byte aligned (they are moved with 16-byte
+ *   vector, cp.async and TMA accesses), except `logits`, which needs only 2-byte
+ *   alignment; int32 / fp32 arrays need 4-byte alignment.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *   stream) and never allocate, free or synchronise.  They can be captured in a
  *   CUDA graph.

@@ -157,3 +157,21 @@ def test_host_rejects_bad_arguments():
     with pytest.raises(mars.MarsError) as e:
         mars.accept(d, 0.5, kn, kn, kc, kc, ln, workspace=small)
     assert e.value.code == 2
+
+
+def test_word_outputs_need_only_4_byte_alignment():
+    """tokens / conf / n_commit / cache_len may be rows of larger arrays (4-byte aligned)."""
+    g = np.random.default_rng(21)
+    logits = synth.Bf16.from_float(g.standard_normal((1, 4, 999), dtype=np.float32))
+    kn, vn, kc, vc = kv_for(1, 4, 1, 64, 16, 22)
+    hist = torch.zeros((5, 1), dtype=torch.int32, device="cuda")
+    lens = torch.zeros((3,), dtype=torch.int32, device="cuda")
+    conf = torch.zeros((3, 4), dtype=torch.float32, device="cuda")
+    toks = torch.zeros((3, 4), dtype=torch.int32, device="cuda")
+    lens[1] = 5
+    t, c, n = mars.accept(dev_bf16(logits), 0.0, dev_bf16(kn), dev_bf16(vn), dev_bf16(kc), dev_bf16(vc),
+                          lens[1:2], tokens=toks[1:2], conf=conf[1:2], n_commit=hist[3])
+    torch.cuda.synchronize()
+    assert int(hist[3].item()) == 4 and int(lens[1].item()) == 9
+    t_o, c_o, _ = oracle.accept(logits.f64, 0.0)
+    assert np.array_equal(toks[1].cpu().numpy(), t_o[0])

@@ -294,12 +294,18 @@ extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, floa
                            int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit, int32_t* status,
                            void* workspace, size_t workspace_bytes, void* stream) {
   using mars_host::aligned16;
+  using mars_host::aligned2;
+  using mars_host::aligned4;
   MARS_HOST_CHECK(batch > 0 && B > 0 && B <= 16 && V > 0 && Hkv > 0 && D > 0 && D % 8 == 0 && D <= 256 && cap > 0,
                   MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(static_cast<long long>(batch) * B <= 65535, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(!isnan(tau), MARS_ERR_INVALID_ARG);
-  const void* ptrs[] = {logits, k_new, v_new, k_cache, v_cache, cache_len, tokens, conf, n_commit, workspace};
-  for (const void* p : ptrs) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  const void* vec16[] = {k_new, v_new, k_cache, v_cache, workspace};
+  for (const void* p : vec16) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  const void* word4[] = {cache_len, tokens, conf, n_commit};
+  for (const void* p : word4) MARS_HOST_CHECK(p != nullptr && aligned4(p), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(logits != nullptr && aligned2(logits), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(status == nullptr || aligned4(status), MARS_ERR_INVALID_ARG);
   const WsLayout l = ws_layout(batch, B, V);
   MARS_HOST_CHECK(workspace_bytes >= l.total, MARS_ERR_WORKSPACE_TOO_SMALL);
   int rc = mars_host::check_device();

@@ -213,4 +213,6 @@ namespace mars_host {
 int check_device();  // MARS_OK or MARS_ERR_UNSUPPORTED_DEVICE / MARS_ERR_CUDA (cached per device)
 int num_sms();       // SM count of the current device (cached)
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 }  // namespace mars_host

@@ -411,8 +411,10 @@ extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const 
   MARS_HOST_CHECK(D == 64 || D == 128, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(cap > 0 && max_len >= 0 && max_len <= cap, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(scale > 0.f && scale < INFINITY, MARS_ERR_INVALID_ARG);
-  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, cache_len, o};
+  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* p : ptrs) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(cache_len != nullptr && mars_host::aligned4(cache_len), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(status == nullptr || mars_host::aligned4(status), MARS_ERR_INVALID_ARG);
   int rc = mars_host::check_device();
   if (rc != MARS_OK) return rc;
 

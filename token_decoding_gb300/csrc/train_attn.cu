@@ -478,7 +478,8 @@ extern "C" int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint1
   MARS_HOST_CHECK(scale > 0.f && scale < INFINITY, MARS_ERR_INVALID_ARG);
   const void* ptrs[] = {q, k, v, o};
   for (const void* p : ptrs) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(lse == nullptr || (reinterpret_cast<uintptr_t>(lse) & 3u) == 0, MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(lse == nullptr || mars_host::aligned4(lse), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(status == nullptr || mars_host::aligned4(status), MARS_ERR_INVALID_ARG);
   const int nq = (L + kBM - 1) / kBM;
   MARS_HOST_CHECK(static_cast<long long>(batch) * Hq * 2 * nq < (1LL << 31), MARS_ERR_INVALID_ARG);
   int rc = mars_host::check_device();
