@@ -43,6 +43,7 @@ extern "C" {
 #define MARS_ERR_WORKSPACE_TOO_SMALL 2 /* workspace smaller than the *_workspace_size() answer */
 #define MARS_ERR_CUDA 3                /* a CUDA runtime call or a launch failed */
 #define MARS_ERR_UNSUPPORTED_DEVICE 4  /* current device is not compute capability 10.3 */
+#define MARS_ERR_SCRATCH_LIMIT 5       /* shape too large for mars_accept_noalloc's fixed scratch */
 
 /* Bits that kernels OR into the device status word. */
 #define MARS_DEV_CAPACITY 1   /* mars_accept: cache_len + n_commit would exceed cap; that sequence was not appended */
@@ -139,6 +140,33 @@ int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau,
                 int Hkv, int D, int cap,
                 int32_t* tokens, float* conf, int32_t* n_commit,
                 int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mars_accept_noalloc - mars_accept for callers that cannot allocate device
+ * memory.  The MARS pages have no counterpart to this call: it exists for
+ * callers such as plugins that only receive the input and output buffers of a
+ * host framework, or serving loops under a fixed memory budget, for which a
+ * cudaMalloc could fail mid-decode and would synchronise the device.
+ *
+ * Same arguments and results as mars_accept, without the workspace.  The
+ * scratch is a 1 MiB array inside the library (a file-scope __device__
+ * array), which every GPU that loads the library holds until the process
+ * exits.  Nothing is allocated or freed by this call.
+ *   - Limits: batch <= 4096 and batch * B <= 4096; larger shapes return
+ *     MARS_ERR_SCRATCH_LIMIT without launching anything.
+ *   - The first call on a device sets the scratch up on that device (it looks
+ *     up the array's device address and zeroes its counters, a synchronous
+ *     step); make that first call before any stream capture begins.
+ *   - All calls in the process share the one array per device and it keeps
+ *     the last call's contents; calls that overlap on the GPU (for example on
+ *     two streams at once) race on it and must be serialised by the caller.
+ */
+int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int V, float tau,
+                        const uint16_t* k_new, const uint16_t* v_new,
+                        uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
+                        int Hkv, int D, int cap,
+                        int32_t* tokens, float* conf, int32_t* n_commit,
+                        int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -26,8 +26,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "mars_accept", "mars_accept_workspace_size", "mars_decode_attn", "mars_status_string",
-        "mars_train_attn", "mars_version"])
+        "mars_accept", "mars_accept_noalloc", "mars_accept_workspace_size", "mars_decode_attn",
+        "mars_status_string", "mars_train_attn", "mars_version"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     lib.mars_status_string.restype = ctypes.c_char_p
-    for code in range(5):
+    for code in range(6):
         assert lib.mars_status_string(code)
     assert b"unknown" in lib.mars_status_string(99)
     assert lib.mars_version() == 100

@@ -39,6 +39,7 @@ _SIGNATURES = {
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
     "mars_accept": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "mars_accept_noalloc": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -211,4 +212,32 @@ def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, worksp
     _call("mars_accept", _ptr(logits), nb, bq, V, float(tau), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
           _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
           _ptr(workspace), workspace.numel(), _stream(stream))
+    return tokens, conf, n_commit
+
+
+def accept_noalloc(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, tokens, conf, n_commit,
+                   status=None, stream=None):
+    """mars_accept for callers that cannot allocate device memory (include/mars.h:
+    mars_accept_noalloc).  Every output buffer is supplied by the caller; the
+    library uses its own fixed scratch, so nothing is allocated here either.
+    Returns (tokens, conf, n_commit); k_cache, v_cache and cache_len are
+    updated in place."""
+    nb, bq, V = logits.shape
+    hkv, d = k_new.shape[2], k_new.shape[3]
+    cap = k_cache.shape[2]
+    dev = logits.device
+    _check(logits, "logits", torch.bfloat16, (nb, bq, V))
+    _check(k_new, "k_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(v_new, "v_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(k_cache, "k_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(cache_len, "cache_len", torch.int32, (nb,), dev)
+    _check(tokens, "tokens", torch.int32, (nb, bq), dev)
+    _check(conf, "conf", torch.float32, (nb, bq), dev)
+    _check(n_commit, "n_commit", torch.int32, (nb,), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_accept_noalloc", _ptr(logits), nb, bq, V, float(tau), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+          _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
+          _stream(stream))
     return tokens, conf, n_commit

@@ -21,6 +21,9 @@
 //   zero again after every call (the partial slots are simply overwritten).
 #include <math.h>
 
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -340,6 +343,122 @@ extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, floa
   a.partials = reinterpret_cast<Partial*>(ws + l.partials);
   a.row_ticket = reinterpret_cast<int32_t*>(ws + l.row_ticket);
   a.seq_ticket = reinterpret_cast<int32_t*>(ws + l.seq_ticket);
+  a.splits = splits;
+  a.chunk_vec = chunk_vec;
+  accept_kernel<<<dim3(splits, rows), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? MARS_OK : MARS_ERR_CUDA;
+}
+
+// ============================================================================
+// mars_accept_noalloc: the same computation with library-owned scratch.
+//
+// Some callers cannot hand the library a workspace: a plugin that only sees
+// the input and output buffers its host framework gives it, or a serving loop
+// running under a fixed device-memory budget, where cudaMalloc could fail in
+// the middle of decoding and would synchronise the whole device.  This entry
+// point allocates nothing.  Its scratch is a file-scope device array of
+// kNoAllocScratchBytes that every GPU loading this library keeps until the
+// process exits.
+//
+// Layout of the array (fixed, so the counters never share bytes with partial
+// results of an earlier call of another shape):
+//   [0, 16 KB)   per-row completion counters   (batch * B <= 4096)
+//   [16, 32 KB)  per-sequence completion counters (batch <= 4096)
+//   [32 KB, 1 MB) per-slice partial results; the number of vocabulary slices
+//                is reduced when batch * B * slices would not fit.
+// The counters are zeroed once, when the array is set up on a device, and
+// every call returns them to zero.
+// ============================================================================
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+constexpr int kNoAllocMaxRows = 4096;
+constexpr int kNoAllocMaxBatch = 4096;
+constexpr size_t kNoAllocRowTicketOff = 0;
+constexpr size_t kNoAllocSeqTicketOff = kNoAllocRowTicketOff + sizeof(int32_t) * kNoAllocMaxRows;
+constexpr size_t kNoAllocPartialOff = kNoAllocSeqTicketOff + sizeof(int32_t) * kNoAllocMaxBatch;
+constexpr size_t kNoAllocPartialSlots = (kNoAllocScratchBytes - kNoAllocPartialOff) / sizeof(Partial);
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_accept_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_scratch[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of g_accept_scratch on the current device.  The first call on
+// a device resolves the address (in host code the array's name is only a
+// host-side stand-in) and zeroes the counters, with that device current.
+int noalloc_scratch(char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MARS_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MARS_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_scratch[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) return MARS_ERR_CUDA;
+    if (cudaMemset(p, 0, kNoAllocPartialOff) != cudaSuccess) return MARS_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MARS_ERR_CUDA;
+    g_noalloc_scratch[dev] = p;
+  }
+  *out = static_cast<char*>(g_noalloc_scratch[dev]);
+  return MARS_OK;
+}
+
+}  // namespace
+
+extern "C" int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int V, float tau,
+                                   const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
+                                   uint16_t* v_cache, int32_t* cache_len, int Hkv, int D, int cap, int32_t* tokens,
+                                   float* conf, int32_t* n_commit, int32_t* status, void* stream) {
+  using mars_host::aligned16;
+  using mars_host::aligned2;
+  using mars_host::aligned4;
+  MARS_HOST_CHECK(batch > 0 && B > 0 && B <= 16 && V > 0 && Hkv > 0 && D > 0 && D % 8 == 0 && D <= 256 && cap > 0,
+                  MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(!isnan(tau), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(batch <= kNoAllocMaxBatch && static_cast<long long>(batch) * B <= kNoAllocMaxRows,
+                  MARS_ERR_SCRATCH_LIMIT);
+  const void* vec16[] = {k_new, v_new, k_cache, v_cache};
+  for (const void* p : vec16) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  const void* word4[] = {cache_len, tokens, conf, n_commit};
+  for (const void* p : word4) MARS_HOST_CHECK(p != nullptr && aligned4(p), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(logits != nullptr && aligned2(logits), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(status == nullptr || aligned4(status), MARS_ERR_INVALID_ARG);
+  int rc = mars_host::check_device();
+  if (rc != MARS_OK) return rc;
+  char* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != MARS_OK) return rc;
+
+  const int rows = batch * B;
+  const int nvec_max = ceil_div(V, 8);
+  const int target_ctas = 16 * mars_host::num_sms();
+  int splits = std::min(max_splits_for(V), std::max(1, ceil_div(target_ctas, rows)));
+  splits = std::max(1, std::min(splits, static_cast<int>(kNoAllocPartialSlots / rows)));
+  const int chunk_vec = ceil_div(nvec_max, splits);
+  splits = ceil_div(nvec_max, chunk_vec);
+
+  AcceptArgs a;
+  a.logits = logits;
+  a.batch = batch;
+  a.B = B;
+  a.V = V;
+  a.tau = tau;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cache_len = cache_len;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.cap = cap;
+  a.tokens = tokens;
+  a.conf = conf;
+  a.n_commit = n_commit;
+  a.status = status;
+  a.partials = reinterpret_cast<Partial*>(scratch + kNoAllocPartialOff);
+  a.row_ticket = reinterpret_cast<int32_t*>(scratch + kNoAllocRowTicketOff);
+  a.seq_ticket = reinterpret_cast<int32_t*>(scratch + kNoAllocSeqTicketOff);
   a.splits = splits;
   a.chunk_vec = chunk_vec;
   accept_kernel<<<dim3(splits, rows), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);

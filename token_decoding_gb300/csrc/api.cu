@@ -50,6 +50,8 @@ extern "C" const char* mars_status_string(int status) {
       return "a CUDA runtime call or kernel launch failed";
     case MARS_ERR_UNSUPPORTED_DEVICE:
       return "the current device is not compute capability 10.3 (GB300, sm_103a)";
+    case MARS_ERR_SCRATCH_LIMIT:
+      return "shape exceeds the fixed scratch of mars_accept_noalloc (batch <= 4096, batch * B <= 4096)";
     default:
       return "unknown status";
   }
