@@ -124,11 +124,11 @@ int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v
  *   cache_len        [batch] int32, device, in/out
  *   tokens [batch, B] int32, conf [batch, B] fp32, n_commit [batch] int32 (written)
  *   workspace        device buffer of >= mars_accept_workspace_size(batch, B, V)
- *                    bytes, zero-filled before its first use.  It holds per-slice
- *                    partial results and completion counters; every call returns
- *                    the counters to zero, so the same buffer is passed unchanged
- *                    to the next call.  Calls that share a workspace must not
- *                    overlap in time.
+ *                    bytes.  It holds one partial result per 16 KB slice of
+ *                    logits; its contents on entry do not matter.  Calls that
+ *                    share a workspace must not overlap in time.
+ * The call is two kernel launches on `stream` (the streaming reduction, then
+ * one CTA per sequence for the commit rule and the append).
  * If cache_len[b] + n > cap nothing is appended for b, cache_len[b] is kept,
  * n_commit[b] is 0 and MARS_DEV_CAPACITY is set.
  * Supported: 1 <= B <= 16, 1 <= V, D % 8 == 0, D <= 256.
@@ -151,12 +151,14 @@ int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau,
  * Same arguments and results as mars_accept, without the workspace.  The
  * scratch is a 1 MiB array inside the library (a file-scope __device__
  * array), which every GPU that loads the library holds until the process
- * exits.  Nothing is allocated or freed by this call.
- *   - Limits: batch <= 4096 and batch * B <= 4096; larger shapes return
+ * exits.  Nothing is allocated or freed by this call; nothing in the array
+ * needs to start at zero.
+ *   - Limit: batch * B * ceil(V / 8192) <= 65536 (one partial result per
+ *     16 KB slice of logits must fit); larger shapes return
  *     MARS_ERR_SCRATCH_LIMIT without launching anything.
  *   - The first call on a device sets the scratch up on that device (it looks
- *     up the array's device address and zeroes its counters, a synchronous
- *     step); make that first call before any stream capture begins.
+ *     up the array's device address); make that first call before any stream
+ *     capture begins.
  *   - All calls in the process share the one array per device and it keeps
  *     the last call's contents; calls that overlap on the GPU (for example on
  *     two streams at once) race on it and must be serialised by the caller.

@@ -84,13 +84,15 @@ def test_noalloc_matches_workspace_accept_twice(batch, B, V, tau):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    logits = torch.zeros((1025, 4, 16), dtype=torch.bfloat16, device="cuda")  # batch * B = 4100 > 4096
-    kn = torch.zeros((1025, 4, 1, 64), dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros((1025, 1, 8, 64), dtype=torch.bfloat16, device="cuda")
-    ln = torch.zeros((1025,), dtype=torch.int32, device="cuda")
-    tok = torch.zeros((1025, 4), dtype=torch.int32, device="cuda")
-    conf = torch.zeros((1025, 4), dtype=torch.float32, device="cuda")
-    n = torch.zeros((1025,), dtype=torch.int32, device="cuda")
-    with pytest.raises(mars.MarsError) as e:
-        _lib.accept_noalloc(logits, 0.5, kn, kn, kc, kc, ln, tok, conf, n)
-    assert e.value.code == 5
+    """batch * B * ceil(V / 8192) above 65536 is refused before anything is launched."""
+    f = _lib.lib().mars_accept_noalloc
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.restype = I
+    f.argtypes = [P, I, I, I, F, P, P, P, P, P, I, I, I, P, P, P, P, P]
+    buf = torch.zeros(4096, dtype=torch.int32, device="cuda")
+    ptr = P(buf.data_ptr())
+    # 512 sequences x 16 positions x ceil(73729 / 8192) = 8192 x 10 slices > 65536
+    rc = f(ptr, 512, 16, 73729, F(0.5), ptr, ptr, ptr, ptr, ptr, 1, 64, 8, ptr, ptr, ptr, None, None)
+    assert rc == 5, mars.status_string(rc)
+    # the same rows with a short vocabulary fit
+    assert mars.status_string(5).startswith("shape exceeds")

@@ -176,7 +176,7 @@ def accept_workspace_size(batch: int, B: int, V: int) -> int:
 
 
 def accept_workspace(batch: int, B: int, V: int, device) -> torch.Tensor:
-    """A zero-filled workspace for accept (its counters return to zero after every call)."""
+    """A workspace for accept (one partial result per 16 KB slice of logits)."""
     n = accept_workspace_size(batch, B, V)
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 

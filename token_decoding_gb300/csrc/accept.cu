@@ -7,18 +7,25 @@
 // Sec. 3.1 gap (4) (strictly left to right) and its block-level KV cache
 // contribution; the aitrends.kr summary (at least one token is accepted).
 //
-// Design (HBM-bound, one read of the logits):
-//   grid = (splits, batch * B).  CTA (s, r) streams a contiguous slice of row
-//   r with 16-byte loads, UNROLL of them in flight per thread, and keeps a
-//   running (max, argmax, sum exp(x - max)) per thread.  The max of each
-//   loaded batch is taken first on packed bf16, so the exponentials are taken
-//   against a running max that rarely moves, and the argmax only needs a scan
-//   when the batch max beats it.  Warp shuffles and shared memory reduce the
-//   CTA; the partial goes to the workspace.  The last CTA of a row (an atomic
-//   ticket, no waiting) merges the partials and writes tokens / conf; the last
-//   row of a sequence computes n_commit and copies the committed K/V rows into
-//   the cache.  Tickets are reset by their last user, so the counters are
-//   zero again after every call (the partial slots are simply overwritten).
+// Design (HBM-bound: one read of the logits, no atomics, no counters):
+//   * Launch 1 (accept_kernel).  Each row (b, i) of logits is cut into 16 KB
+//     chunks; a chunk is one work item.  CTAs are persistent, one per SM: CTA c
+//     takes items c, c + grid, ...  A producer warp streams the CTA's chunks
+//     with 1-D bulk copies (cp.async.bulk) into a ring of kSlots 16 KB
+//     shared-memory slots guarded by full/empty mbarriers (~190 KB in flight
+//     per SM).  Consumer warp w owns slot w and takes every kSlots-th chunk:
+//     its lanes read 16-byte vectors from the slot, take the group max on
+//     packed bf16, keep the group that raised the running max in registers
+//     (one argmax scan per lane and chunk), and accumulate
+//     sum exp2(x*log2e - max*log2e) with packed fp32x2 FMA/ADD.  The slot is
+//     released as soon as it is read; the warp reduces with shuffles and
+//     stores the chunk's (max, argmax, sum) partial.
+//   * Launch 2 (accept_finish_kernel, programmatic dependent launch: it starts
+//     while launch 1 runs, prefetches cache_len and the candidate K/V rows, and
+//     waits in-kernel for the partials), one CTA per sequence: each warp merges
+//     one row's partials and writes tokens / conf, a ballot over the B
+//     confidences gives the commit count, and the committed K/V rows are
+//     copied into the cache.
 #include <math.h>
 
 #include <algorithm>
@@ -30,10 +37,12 @@ namespace {
 
 using namespace mars;
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;          // 16-byte loads in flight per thread
-constexpr int kMinChunkVec = 256;   // smallest slice per CTA, in 16-byte vectors (4 KB)
+constexpr int kChunkVec = 1024;                 // 16-byte vectors per chunk (16 KB)
+constexpr int kSlots = 12;                      // ring slots = consumer warps
+constexpr int kThreads = 32 * (kSlots + 1);     // + one producer warp
+constexpr int kRingBytes = kSlots * kChunkVec * 16;
+constexpr int kGroup = 4;                       // vectors per lane per step
+constexpr int kSteps = kChunkVec / (32 * kGroup);
 
 struct RowState {
   float m;   // running max (-inf when empty)
@@ -77,29 +86,39 @@ __device__ __forceinline__ RowState shfl_state(const RowState& a, int lane_mask)
   return b;
 }
 
-// Add one scalar element (index increasing is NOT assumed).
-__device__ __forceinline__ void add_scalar(RowState& st, float x, int idx) {
-  RowState one{x, idx, 1.f};
-  merge(st, one);
+__device__ __forceinline__ RowState warp_reduce(RowState st) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_state(st, o));
+  return st;
 }
+
+// Add one scalar element (index order not assumed).
+__device__ __forceinline__ void add_scalar(RowState& st, float x, int idx) { merge(st, RowState{x, idx, 1.f}); }
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-__device__ __forceinline__ RowState block_reduce(RowState st, RowState* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) merge(st, shfl_state(st, o));
-  if (lane == 0) red[warp] = st;
-  __syncthreads();
-  if (warp == 0) {
-    st = lane < kWarps ? red[lane] : empty_state();
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) merge(st, shfl_state(st, o));
-  }
-  return st;  // valid in thread 0
+// acc2 (+)= exp2(x * log2e + mneg) for the two bf16 values packed in w, using
+// packed fp32x2 FMA / ADD so one instruction serves both halves.
+__device__ __forceinline__ void exp2_accumulate_pair(uint64_t& acc2, uint32_t w, float mneg) {
+  const float lo = bf16lo_to_f32(w), hi = bf16hi_to_f32(w);
+  float t0, t1;
+  asm("{\n .reg .b64 x, c, b, t;\n mov.b64 x, {%2, %3};\n mov.b64 c, {%4, %4};\n mov.b64 b, {%5, %5};\n"
+      " fma.rn.f32x2 t, x, c, b;\n mov.b64 {%0, %1}, t;\n}\n"
+      : "=f"(t0), "=f"(t1)
+      : "f"(lo), "f"(hi), "f"(kLog2e), "f"(mneg));
+  const float e0 = fast_exp2(t0), e1 = fast_exp2(t1);
+  asm("{\n .reg .b64 e;\n mov.b64 e, {%1, %2};\n add.rn.f32x2 %0, %0, e;\n}\n" : "+l"(acc2) : "f"(e0), "f"(e1));
+}
+__device__ __forceinline__ uint64_t pair_scale(uint64_t acc2, float f) {
+  uint64_t r;
+  asm("{\n .reg .b64 c;\n mov.b64 c, {%2, %2};\n mul.rn.f32x2 %0, %1, c;\n}\n" : "=l"(r) : "l"(acc2), "f"(f));
+  return r;
+}
+__device__ __forceinline__ float pair_sum(uint64_t acc2) {
+  return __uint_as_float(static_cast<uint32_t>(acc2)) + __uint_as_float(static_cast<uint32_t>(acc2 >> 32));
 }
 
 struct AcceptArgs {
@@ -116,212 +135,292 @@ struct AcceptArgs {
   float* conf;
   int32_t* n_commit;
   int32_t* status;
-  Partial* partials;    // [rows][splits]
-  int32_t* row_ticket;  // [rows]
-  int32_t* seq_ticket;  // [batch]
-  int splits;
-  int chunk_vec;        // vectors per CTA slice
+  Partial* partials;    // [rows][chunks]
+  int chunks;           // chunks per row
+  int items;            // rows * chunks
 };
 
-__global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptArgs a) {
-  __shared__ RowState red[kWarps];
-  __shared__ int flag;
+// Chunk k of row r: aligned vectors [v0, v1) plus the row's scalar head/tail bounds.
+struct Chunk {
+  const uint16_t* row;
+  int head, tail0, v0, v1;
+};
 
-  const int split = blockIdx.x;
-  const int r = blockIdx.y;  // row = b * B + i
-  const int tid = threadIdx.x;
-  const uint16_t* row = a.logits + static_cast<size_t>(r) * a.V;
+__device__ __forceinline__ Chunk chunk_of(const AcceptArgs& a, int r, int k) {
+  Chunk c;
+  c.row = a.logits + static_cast<size_t>(r) * a.V;
+  // Elements [0, head) and [tail0, V) are not 16-byte aligned and are read as scalars.
+  c.head = min(static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(c.row) & 15u)) & 15u) >> 1), a.V);
+  const int nvec = (a.V - c.head) >> 3;
+  c.tail0 = c.head + 8 * nvec;
+  c.v0 = min(nvec, k * kChunkVec);
+  c.v1 = min(nvec, c.v0 + kChunkVec);
+  return c;
+}
 
-  // Elements [0, head) and [head + 8 * nvec, V) are not 16-byte aligned and are read as scalars.
-  const int head = min(static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) >> 1), a.V);
-  const int nvec = (a.V - head) >> 3;
-  const int tail0 = head + 8 * nvec;
-  const int v0 = split * a.chunk_vec;
-  const int v1 = min(nvec, v0 + a.chunk_vec);
+// Second launch: one CTA per sequence b, one warp per proposal position i.
+// Warp i merges the chunk partials of row (b, i) and writes tokens / conf;
+// then the leading positions with conf >= tau are counted from a ballot (at
+// least one), and the committed K/V rows are copied into the cache.  The
+// partials, cache_len and (up to kPrefetch vectors per thread of) the B
+// candidate K/V rows are all requested up front, so the launch costs about
+// one memory round trip plus the stores.
+constexpr int kPrefetch = 4;
 
-  RowState st = empty_state();
-  // ---- vector body: thread-local indices increase monotonically
-  {
-    const uint4* vp = reinterpret_cast<const uint4*>(row + head);
-    float m = -INFINITY, mneg = 0.f, s0 = 0.f, s1 = 0.f;
-    int idx = 0x7fffffff;
-    for (int base = v0 + tid; base < v1; base += kThreads * kUnroll) {
-      uint4 w[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int vi = base + u * kThreads;
-        w[u] = vi < v1 ? __ldcs(vp + vi) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-      }
-      uint32_t mx = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
-#pragma unroll
-      for (int u = 1; u < kUnroll; ++u) mx = bmax2(mx, bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w)));
-      const float gmax = fmaxf(bf16lo_to_f32(mx), bf16hi_to_f32(mx));
-      if (gmax > m) {
-        // first element equal to the new max, in index order
-        int found = 0x7fffffff;
-#pragma unroll
-        for (int u = kUnroll - 1; u >= 0; --u) {
-          const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-#pragma unroll
-          for (int e = 7; e >= 0; --e) {
-            const float x = (e & 1) ? bf16hi_to_f32(ws[e >> 1]) : bf16lo_to_f32(ws[e >> 1]);
-            if (x == gmax) found = head + 8 * (base + u * kThreads) + e;
-          }
-        }
-        const float f = fast_exp2((m - gmax) * kLog2e);
-        s0 *= f;
-        s1 *= f;
-        m = gmax;
-        mneg = -gmax * kLog2e;
-        idx = found;
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          s0 += fast_exp2(fmaf(bf16lo_to_f32(ws[h]), kLog2e, mneg));
-          s1 += fast_exp2(fmaf(bf16hi_to_f32(ws[h]), kLog2e, mneg));
-        }
-      }
-    }
-    st.m = m;
-    st.idx = idx;
-    st.s = s0 + s1;
-    if (m == -INFINITY) st = empty_state();
-  }
-  // ---- unaligned head (split 0) and tail (last split): at most 7 + 7 elements
-  if (split == 0 && tid < head) add_scalar(st, bf16lo_to_f32(row[tid]), tid);
-  if (split == a.splits - 1 && tail0 + tid < a.V) add_scalar(st, bf16lo_to_f32(row[tail0 + tid]), tail0 + tid);
-
-  st = block_reduce(st, red);
-
-  // ---- row finalisation: by the only CTA (splits == 1) or the last one to finish
-  if (tid == 0) {
-    int last = 1;
-    if (a.splits > 1) {
-      a.partials[static_cast<size_t>(r) * a.splits + split] = Partial{st.m, st.idx, st.s, 0};
-      __threadfence();
-      last = atomicAdd(&a.row_ticket[r], 1) == a.splits - 1;
-      if (last) {
-        __threadfence();
-        st = empty_state();
-        for (int s = 0; s < a.splits; ++s) {
-          const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partials + static_cast<size_t>(r) * a.splits + s));
-          merge(st, RowState{p.x, __float_as_int(p.y), p.z});
-        }
-        a.row_ticket[r] = 0;
-      }
-    }
-    int seq_last = 0;
-    if (last) {
-      a.tokens[r] = st.idx;
-      a.conf[r] = 1.0f / st.s;
-      __threadfence();
-      const int b = r / a.B;
-      seq_last = atomicAdd(&a.seq_ticket[b], 1) == a.B - 1;
-      if (seq_last) __threadfence();
-    }
-    flag = seq_last;
-  }
-  __syncthreads();
-  if (!flag) return;
-
-  // ---- sequence finalisation: commit count and KV append
+__global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs a) {
+  __shared__ float s_conf[16];
   __shared__ int s_n, s_len;
-  const int b = r / a.B;
-  if (tid == 0) {
-    int n = 0;
-    for (int i = 0; i < a.B; ++i) {
-      if (__ldcg(a.conf + b * a.B + i) >= a.tau) ++n;
-      else break;
-    }
-    n = max(n, 1);
-    const int len = __ldcg(a.cache_len + b);
-    if (len < 0 || len + n > a.cap) {
-      set_status(a.status, MARS_DEV_CAPACITY);
-      n = 0;
-    }
-    a.n_commit[b] = n;
-    s_n = n;
-    s_len = len;
-    a.seq_ticket[b] = 0;
-  }
-  __syncthreads();
-  const int n = s_n, len = s_len;
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vec_per_row = a.D >> 3;
   const int per_pos = a.Hkv * vec_per_row;
-  const int total = n * per_pos;
-  for (int e = tid; e < total; e += kThreads) {
+  const int cand = a.B * per_pos;  // candidate 16-byte vectors of K (and of V)
+  const int len0 = __ldg(a.cache_len + b);
+  uint4 kpre[kPrefetch], vpre[kPrefetch];
+#pragma unroll
+  for (int u = 0; u < kPrefetch; ++u) {
+    const int e = threadIdx.x + u * blockDim.x;
+    if (e < cand) {
+      const size_t src = (static_cast<size_t>(b) * a.B * per_pos + e) * 8;  // rows of [B, Hkv, D] are contiguous
+      kpre[u] = *reinterpret_cast<const uint4*>(a.k_new + src);
+      vpre[u] = *reinterpret_cast<const uint4*>(a.v_new + src);
+    }
+  }
+  griddep_wait();  // the streaming launch's partials are complete and visible from here on
+  {
+    const int r = b * a.B + warp;
+    RowState mg = empty_state();
+    for (int s = lane; s < a.chunks; s += 32) {
+      const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partials + static_cast<size_t>(r) * a.chunks + s));
+      merge(mg, RowState{p.x, __float_as_int(p.y), p.z});
+    }
+    const RowState st = warp_reduce(mg);
+    if (lane == 0) {
+      const float conf = 1.0f / st.s;
+      a.tokens[r] = st.idx;
+      a.conf[r] = conf;
+      s_conf[warp] = conf;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const bool pass = lane < a.B && s_conf[min(lane, a.B - 1)] >= a.tau;
+    const uint32_t ok = __ballot_sync(0xffffffffu, pass);
+    if (lane == 0) {
+      int n = max(min(__ffs(~ok) - 1, a.B), 1);
+      if (len0 < 0 || len0 + n > a.cap) {
+        set_status(a.status, MARS_DEV_CAPACITY);
+        n = 0;
+      }
+      s_n = n;
+      a.n_commit[b] = n;
+      a.cache_len[b] = len0 + n;
+    }
+  }
+  __syncthreads();
+  // ---- block-level KV append of the committed rows: candidate vector e is
+  // (position i, head g, chunk c) with e = (i * Hkv + g) * vec_per_row + c
+  const int n = s_n;
+  auto store = [&](int e, const uint4& kv, const uint4& vv) {
     const int i = e / per_pos;
     const int g = (e / vec_per_row) % a.Hkv;
     const int c = e % vec_per_row;
-    const size_t src = ((static_cast<size_t>(b) * a.B + i) * a.Hkv + g) * a.D + 8 * c;
-    const size_t dst = ((static_cast<size_t>(b) * a.Hkv + g) * a.cap + len + i) * a.D + 8 * c;
-    *reinterpret_cast<uint4*>(a.k_cache + dst) = *reinterpret_cast<const uint4*>(a.k_new + src);
-    *reinterpret_cast<uint4*>(a.v_cache + dst) = *reinterpret_cast<const uint4*>(a.v_new + src);
+    const size_t dst = ((static_cast<size_t>(b) * a.Hkv + g) * a.cap + len0 + i) * a.D + 8 * c;
+    *reinterpret_cast<uint4*>(a.k_cache + dst) = kv;
+    *reinterpret_cast<uint4*>(a.v_cache + dst) = vv;
+  };
+#pragma unroll
+  for (int u = 0; u < kPrefetch; ++u) {
+    const int e = threadIdx.x + u * blockDim.x;
+    if (e < n * per_pos) store(e, kpre[u], vpre[u]);
   }
-  if (tid == 0) a.cache_len[b] = len + n;
+  for (int e = threadIdx.x + kPrefetch * blockDim.x; e < n * per_pos; e += blockDim.x) {
+    const size_t src = (static_cast<size_t>(b) * a.B * per_pos + e) * 8;
+    store(e, *reinterpret_cast<const uint4*>(a.k_new + src), *reinterpret_cast<const uint4*>(a.v_new + src));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a) {
+  extern __shared__ __align__(128) uint4 ring[];  // [kSlots][kChunkVec]
+  __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_launch_dependents();  // the finish launch may start prefetching beside us
+
+  if (warp == kSlots) {
+    // ================= producer: the CTA's chunks, in order, through the ring
+    if (lane == 0) {
+      int j = 0;  // CTA-local chunk sequence number; slot = j % kSlots
+      for (int item = blockIdx.x; item < a.items; item += gridDim.x, ++j) {
+        const int slot = j % kSlots;
+        if (j >= kSlots && !mbar_wait(&empty[slot], ((j / kSlots) - 1) & 1)) {
+          set_status(a.status, MARS_DEV_TIMEOUT);
+          return;
+        }
+        const Chunk c = chunk_of(a, item / a.chunks, item % a.chunks);
+        const uint32_t bytes = static_cast<uint32_t>(c.v1 - c.v0) * 16u;
+        mbar_arrive_expect_tx(&full[slot], bytes);  // bytes == 0 completes the phase at once
+        if (bytes > 0)
+          bulk_g2s(smem_u32(ring + slot * kChunkVec), reinterpret_cast<const uint4*>(c.row + c.head) + c.v0, bytes,
+                   &full[slot]);
+      }
+    }
+    return;
+  }
+
+  // ================= consumer warp `warp`: chunks j = warp, warp + kSlots, ...
+  const uint4 kNegInf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  const uint4* buf = ring + warp * kChunkVec;
+  int j = warp;
+  for (int item = blockIdx.x + warp * gridDim.x; item < a.items; item += kSlots * gridDim.x, j += kSlots) {
+    const int r = item / a.chunks, k = item % a.chunks;
+    const Chunk c = chunk_of(a, r, k);
+    if (!mbar_wait(&full[warp], (j / kSlots) & 1)) {
+      if (lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+      return;
+    }
+    const int n = c.v1 - c.v0;
+
+    // ---- the chunk: lane l reads vectors l + 32 * (kGroup * step + u), index order per lane
+    float m = -INFINITY, mneg = 0.f;
+    uint64_t acc2 = 0;
+    int best_step = -1;
+    uint4 best[kGroup];
+#pragma unroll 2
+    for (int step = 0; step < kSteps; ++step) {
+      uint4 w[kGroup];
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int vi = lane + 32 * (kGroup * step + u);
+        w[u] = vi < n ? buf[vi] : kNegInf;
+      }
+      uint32_t mx = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
+#pragma unroll
+      for (int u = 1; u < kGroup; ++u) mx = bmax2(mx, bmax2(bmax2(w[u].x, w[u].y), bmax2(w[u].z, w[u].w)));
+      const float gmax = fmaxf(bf16lo_to_f32(mx), bf16hi_to_f32(mx));
+      if (gmax > m) {
+        acc2 = pair_scale(acc2, fast_exp2((m - gmax) * kLog2e));  // exp2(-inf) = 0 on the first group
+        m = gmax;
+        mneg = -gmax * kLog2e;
+        best_step = step;
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) best[u] = w[u];
+      }
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        exp2_accumulate_pair(acc2, w[u].x, mneg);
+        exp2_accumulate_pair(acc2, w[u].y, mneg);
+        exp2_accumulate_pair(acc2, w[u].z, mneg);
+        exp2_accumulate_pair(acc2, w[u].w, mneg);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[warp]);  // the slot is free again
+
+    RowState st = empty_state();
+    if (best_step >= 0) {
+      int found = 0x7fffffff;
+#pragma unroll
+      for (int u = kGroup - 1; u >= 0; --u) {
+        const uint32_t ws[4] = {best[u].x, best[u].y, best[u].z, best[u].w};
+#pragma unroll
+        for (int e = 7; e >= 0; --e) {
+          const float x = (e & 1) ? bf16hi_to_f32(ws[e >> 1]) : bf16lo_to_f32(ws[e >> 1]);
+          if (x == m) found = c.head + 8 * (c.v0 + lane + 32 * (kGroup * best_step + u)) + e;
+        }
+      }
+      st = RowState{m, found, pair_sum(acc2)};
+    }
+    // ---- unaligned head (first chunk) and tail (last chunk): at most 7 + 7 elements
+    if (k == 0 && lane < c.head) add_scalar(st, bf16lo_to_f32(c.row[lane]), lane);
+    if (k == a.chunks - 1 && c.tail0 + lane < a.V) add_scalar(st, bf16lo_to_f32(c.row[c.tail0 + lane]), c.tail0 + lane);
+    st = warp_reduce(st);
+    if (lane == 0) a.partials[static_cast<size_t>(r) * a.chunks + k] = Partial{st.m, st.idx, st.s, 0};
+  }
+
 }
 
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Number of 16-byte vectors per row that a CTA slice can cover at most.
-inline int max_splits_for(int V) { return max(1, ceil_div(ceil_div(V, 8), kMinChunkVec)); }
+// Chunks per row of V logits (a row's aligned part has at most ceil(V/8) vectors).
+inline int chunks_for(int V) { return max(1, ceil_div(ceil_div(V, 8), kChunkVec)); }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-struct WsLayout {
-  size_t partials, row_ticket, seq_ticket, total;
-};
-
-inline WsLayout ws_layout(int batch, int B, int V) {
-  const size_t rows = static_cast<size_t>(batch) * B;
-  WsLayout l;
-  l.partials = 0;
-  l.row_ticket = align_up(rows * max_splits_for(V) * sizeof(Partial), 256);
-  l.seq_ticket = align_up(l.row_ticket + rows * sizeof(int32_t), 256);
-  l.total = align_up(l.seq_ticket + static_cast<size_t>(batch) * sizeof(int32_t), 256);
-  return l;
+// Workspace: one Partial per (row, chunk).
+inline size_t ws_bytes(int batch, int B, int V) {
+  return align_up(static_cast<size_t>(batch) * B * chunks_for(V) * sizeof(Partial), 256);
 }
 
-}  // namespace
-
-extern "C" size_t mars_accept_workspace_size(int batch, int B, int V) {
-  if (batch <= 0 || B <= 0 || V <= 0) return 0;
-  return ws_layout(batch, B, V).total;
+int configure_kernel() {
+  static int done[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MARS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes) != cudaSuccess)
+      return MARS_ERR_CUDA;
+    done[dev] = 1;
+  }
+  return MARS_OK;
 }
 
-extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
-                           const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len, int Hkv,
-                           int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit, int32_t* status,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+int launch(AcceptArgs& a, cudaStream_t stream) {
+  const int rc = configure_kernel();
+  if (rc != MARS_OK) return rc;
+  a.chunks = chunks_for(a.V);
+  a.items = a.batch * a.B * a.chunks;
+  const int grid = std::min(a.items, mars_host::num_sms());
+  accept_kernel<<<grid, kThreads, kRingBytes, stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return MARS_ERR_CUDA;
+  // The finish launch overlaps its start-up and prefetch with the streaming launch
+  // (programmatic dependent launch); it waits for the partials in-kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.batch, 1, 1);
+  cfg.blockDim = dim3(32 * a.B, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, accept_finish_kernel, a) == cudaSuccess ? MARS_OK : MARS_ERR_CUDA;
+}
+
+// Host-side argument checks shared by both entry points.
+int check_args(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
+               const uint16_t* v_new, const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* cache_len,
+               int Hkv, int D, int cap, const int32_t* tokens, const float* conf, const int32_t* n_commit,
+               const int32_t* status) {
   using mars_host::aligned16;
   using mars_host::aligned2;
   using mars_host::aligned4;
   MARS_HOST_CHECK(batch > 0 && B > 0 && B <= 16 && V > 0 && Hkv > 0 && D > 0 && D % 8 == 0 && D <= 256 && cap > 0,
                   MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(static_cast<long long>(batch) * B <= 65535, MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(static_cast<long long>(batch) * B * chunks_for(V) < (1LL << 31), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(!isnan(tau), MARS_ERR_INVALID_ARG);
-  const void* vec16[] = {k_new, v_new, k_cache, v_cache, workspace};
+  const void* vec16[] = {k_new, v_new, k_cache, v_cache};
   for (const void* p : vec16) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
   const void* word4[] = {cache_len, tokens, conf, n_commit};
   for (const void* p : word4) MARS_HOST_CHECK(p != nullptr && aligned4(p), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(logits != nullptr && aligned2(logits), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(status == nullptr || aligned4(status), MARS_ERR_INVALID_ARG);
-  const WsLayout l = ws_layout(batch, B, V);
-  MARS_HOST_CHECK(workspace_bytes >= l.total, MARS_ERR_WORKSPACE_TOO_SMALL);
-  int rc = mars_host::check_device();
-  if (rc != MARS_OK) return rc;
+  return MARS_OK;
+}
 
-  const int rows = batch * B;
-  const int nvec_max = ceil_div(V, 8);
-  const int target_ctas = 16 * mars_host::num_sms();
-  int splits = std::min(max_splits_for(V), std::max(1, ceil_div(target_ctas, rows)));
-  const int chunk_vec = ceil_div(nvec_max, splits);
-  splits = ceil_div(nvec_max, chunk_vec);
-
-  char* ws = static_cast<char*>(workspace);
+AcceptArgs make_args(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
+                     const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len, int Hkv, int D,
+                     int cap, int32_t* tokens, float* conf, int32_t* n_commit, int32_t* status) {
   AcceptArgs a;
   a.logits = logits;
   a.batch = batch;
@@ -340,13 +439,34 @@ extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, floa
   a.conf = conf;
   a.n_commit = n_commit;
   a.status = status;
-  a.partials = reinterpret_cast<Partial*>(ws + l.partials);
-  a.row_ticket = reinterpret_cast<int32_t*>(ws + l.row_ticket);
-  a.seq_ticket = reinterpret_cast<int32_t*>(ws + l.seq_ticket);
-  a.splits = splits;
-  a.chunk_vec = chunk_vec;
-  accept_kernel<<<dim3(splits, rows), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? MARS_OK : MARS_ERR_CUDA;
+  a.partials = nullptr;
+  a.chunks = a.items = 0;
+  return a;
+}
+
+}  // namespace
+
+extern "C" size_t mars_accept_workspace_size(int batch, int B, int V) {
+  if (batch <= 0 || B <= 0 || V <= 0) return 0;
+  return ws_bytes(batch, B, V);
+}
+
+extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
+                           const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len, int Hkv,
+                           int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit, int32_t* status,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                      conf, n_commit, status);
+  if (rc != MARS_OK) return rc;
+  MARS_HOST_CHECK(workspace != nullptr && mars_host::aligned16(workspace), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(workspace_bytes >= ws_bytes(batch, B, V), MARS_ERR_WORKSPACE_TOO_SMALL);
+  rc = mars_host::check_device();
+  if (rc != MARS_OK) return rc;
+
+  AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                           conf, n_commit, status);
+  a.partials = static_cast<Partial*>(workspace);
+  return launch(a, static_cast<cudaStream_t>(stream));
 }
 
 // ============================================================================
@@ -360,24 +480,14 @@ extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, floa
 // kNoAllocScratchBytes that every GPU loading this library keeps until the
 // process exits.
 //
-// Layout of the array (fixed, so the counters never share bytes with partial
-// results of an earlier call of another shape):
-//   [0, 16 KB)   per-row completion counters   (batch * B <= 4096)
-//   [16, 32 KB)  per-sequence completion counters (batch <= 4096)
-//   [32 KB, 1 MB) per-slice partial results; the number of vocabulary slices
-//                is reduced when batch * B * slices would not fit.
-// The counters are zeroed once, when the array is set up on a device, and
-// every call returns them to zero.
+// The array holds only the per-chunk partial results of the current call
+// (batch * B * ceil(V / 8192) of them, at most 65536); nothing in it has to
+// start at zero, and each call overwrites what it reads.
 // ============================================================================
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
-constexpr int kNoAllocMaxRows = 4096;
-constexpr int kNoAllocMaxBatch = 4096;
-constexpr size_t kNoAllocRowTicketOff = 0;
-constexpr size_t kNoAllocSeqTicketOff = kNoAllocRowTicketOff + sizeof(int32_t) * kNoAllocMaxRows;
-constexpr size_t kNoAllocPartialOff = kNoAllocSeqTicketOff + sizeof(int32_t) * kNoAllocMaxBatch;
-constexpr size_t kNoAllocPartialSlots = (kNoAllocScratchBytes - kNoAllocPartialOff) / sizeof(Partial);
+constexpr size_t kNoAllocPartialSlots = kNoAllocScratchBytes / sizeof(Partial);
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_accept_scratch[kNoAllocScratchBytes];
@@ -386,8 +496,8 @@ void* g_noalloc_scratch[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
 
 // Device address of g_accept_scratch on the current device.  The first call on
-// a device resolves the address (in host code the array's name is only a
-// host-side stand-in) and zeroes the counters, with that device current.
+// a device resolves the address with that device current (in host code the
+// array's name is only a host-side stand-in, not a device address).
 int noalloc_scratch(char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MARS_ERR_CUDA;
@@ -396,8 +506,6 @@ int noalloc_scratch(char** out) {
   if (g_noalloc_scratch[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) return MARS_ERR_CUDA;
-    if (cudaMemset(p, 0, kNoAllocPartialOff) != cudaSuccess) return MARS_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return MARS_ERR_CUDA;
     g_noalloc_scratch[dev] = p;
   }
   *out = static_cast<char*>(g_noalloc_scratch[dev]);
@@ -410,57 +518,20 @@ extern "C" int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int
                                    const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
                                    uint16_t* v_cache, int32_t* cache_len, int Hkv, int D, int cap, int32_t* tokens,
                                    float* conf, int32_t* n_commit, int32_t* status, void* stream) {
-  using mars_host::aligned16;
-  using mars_host::aligned2;
-  using mars_host::aligned4;
-  MARS_HOST_CHECK(batch > 0 && B > 0 && B <= 16 && V > 0 && Hkv > 0 && D > 0 && D % 8 == 0 && D <= 256 && cap > 0,
-                  MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(!isnan(tau), MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(batch <= kNoAllocMaxBatch && static_cast<long long>(batch) * B <= kNoAllocMaxRows,
+  MARS_HOST_CHECK(batch > 0 && B > 0 && V > 0, MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(static_cast<long long>(batch) * B * chunks_for(V) <= static_cast<long long>(kNoAllocPartialSlots),
                   MARS_ERR_SCRATCH_LIMIT);
-  const void* vec16[] = {k_new, v_new, k_cache, v_cache};
-  for (const void* p : vec16) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
-  const void* word4[] = {cache_len, tokens, conf, n_commit};
-  for (const void* p : word4) MARS_HOST_CHECK(p != nullptr && aligned4(p), MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(logits != nullptr && aligned2(logits), MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(status == nullptr || aligned4(status), MARS_ERR_INVALID_ARG);
-  int rc = mars_host::check_device();
+  int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                      conf, n_commit, status);
+  if (rc != MARS_OK) return rc;
+  rc = mars_host::check_device();
   if (rc != MARS_OK) return rc;
   char* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
   if (rc != MARS_OK) return rc;
 
-  const int rows = batch * B;
-  const int nvec_max = ceil_div(V, 8);
-  const int target_ctas = 16 * mars_host::num_sms();
-  int splits = std::min(max_splits_for(V), std::max(1, ceil_div(target_ctas, rows)));
-  splits = std::max(1, std::min(splits, static_cast<int>(kNoAllocPartialSlots / rows)));
-  const int chunk_vec = ceil_div(nvec_max, splits);
-  splits = ceil_div(nvec_max, chunk_vec);
-
-  AcceptArgs a;
-  a.logits = logits;
-  a.batch = batch;
-  a.B = B;
-  a.V = V;
-  a.tau = tau;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.cache_len = cache_len;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.cap = cap;
-  a.tokens = tokens;
-  a.conf = conf;
-  a.n_commit = n_commit;
-  a.status = status;
-  a.partials = reinterpret_cast<Partial*>(scratch + kNoAllocPartialOff);
-  a.row_ticket = reinterpret_cast<int32_t*>(scratch + kNoAllocRowTicketOff);
-  a.seq_ticket = reinterpret_cast<int32_t*>(scratch + kNoAllocSeqTicketOff);
-  a.splits = splits;
-  a.chunk_vec = chunk_vec;
-  accept_kernel<<<dim3(splits, rows), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? MARS_OK : MARS_ERR_CUDA;
+  AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                           conf, n_commit, status);
+  a.partials = reinterpret_cast<Partial*>(scratch);
+  return launch(a, static_cast<cudaStream_t>(stream));
 }

@@ -51,7 +51,7 @@ extern "C" const char* mars_status_string(int status) {
     case MARS_ERR_UNSUPPORTED_DEVICE:
       return "the current device is not compute capability 10.3 (GB300, sm_103a)";
     case MARS_ERR_SCRATCH_LIMIT:
-      return "shape exceeds the fixed scratch of mars_accept_noalloc (batch <= 4096, batch * B <= 4096)";
+      return "shape exceeds the fixed scratch of mars_accept_noalloc (batch * B * ceil(V / 8192) <= 65536)";
     default:
       return "unknown status";
   }
