@@ -53,6 +53,10 @@ extern "C" {
 /* Human-readable text for a return code (static storage, never NULL). */
 const char* mars_status_string(int status);
 
+/* Text of the CUDA error behind the calling thread's last MARS_ERR_CUDA
+ * ("no error" if there was none); static storage, never NULL. */
+const char* mars_last_cuda_error(void);
+
 /* Library ABI version: 100 * major + minor. */
 int mars_version(void);
 

@@ -35,6 +35,7 @@ _SZ = ctypes.c_size_t
 _SIGNATURES = {
     "mars_status_string": (ctypes.c_char_p, [_I]),
     "mars_version": (_I, []),
+    "mars_last_cuda_error": (ctypes.c_char_p, []),
     "mars_train_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
@@ -47,7 +48,8 @@ _lib = None
 
 class MarsError(RuntimeError):
     def __init__(self, fn, code):
-        super().__init__(f"{fn} failed: {code} ({status_string(code)})")
+        detail = f"; CUDA: {last_cuda_error()}" if code == MARS_ERR_CUDA else ""
+        super().__init__(f"{fn} failed: {code} ({status_string(code)}){detail}")
         self.code = code
 
 
@@ -80,6 +82,10 @@ def _fn(name):
 
 def status_string(code: int) -> str:
     return _fn("mars_status_string")(int(code)).decode()
+
+
+def last_cuda_error() -> str:
+    return _fn("mars_last_cuda_error")().decode()
 
 
 def version() -> int:

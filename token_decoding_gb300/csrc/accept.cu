@@ -367,8 +367,8 @@ int configure_kernel() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MARS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes) != cudaSuccess)
-      return MARS_ERR_CUDA;
+    const cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
     done[dev] = 1;
   }
   return MARS_OK;
@@ -381,7 +381,7 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
   a.items = a.batch * a.B * a.chunks;
   const int grid = std::min(a.items, mars_host::num_sms());
   accept_kernel<<<grid, kThreads, kRingBytes, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return MARS_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return mars_host::launch_status();
   // The finish launch overlaps its start-up and prefetch with the streaming launch
   // (programmatic dependent launch); it waits for the partials in-kernel.
   cudaLaunchConfig_t cfg = {};
@@ -394,7 +394,8 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, accept_finish_kernel, a) == cudaSuccess ? MARS_OK : MARS_ERR_CUDA;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_finish_kernel, a);
+  return e == cudaSuccess ? MARS_OK : mars_host::cuda_fail(e);
 }
 
 // Host-side argument checks shared by both entry points.
@@ -505,7 +506,8 @@ int noalloc_scratch(char** out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_scratch[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) return MARS_ERR_CUDA;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (e != cudaSuccess || p == nullptr) return mars_host::cuda_fail(e);
     g_noalloc_scratch[dev] = p;
   }
   *out = static_cast<char*>(g_noalloc_scratch[dev]);

@@ -10,7 +10,21 @@ int g_sms[kMaxDevices];
 std::mutex g_mu;
 }  // namespace
 
+namespace {
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+}  // namespace
+
 namespace mars_host {
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = e;
+  return MARS_ERR_CUDA;
+}
+
+int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MARS_OK : cuda_fail(e);
+}
 
 int check_device() {
   int dev = 0;
@@ -58,3 +72,7 @@ extern "C" const char* mars_status_string(int status) {
 }
 
 extern "C" int mars_version(void) { return 100; }
+
+extern "C" const char* mars_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
+}

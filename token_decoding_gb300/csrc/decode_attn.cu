@@ -364,9 +364,8 @@ int launch(const DecodeArgs& a, int units, cudaStream_t stream) {
   const size_t smem = smem_bytes<D, NW>();
   static bool configured = false;  // per instantiation; the attribute is process-wide
   if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-      return MARS_ERR_CUDA;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -381,7 +380,8 @@ int launch(const DecodeArgs& a, int units, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return MARS_ERR_CUDA;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return mars_host::cuda_fail(e);
   return MARS_OK;
 }
 

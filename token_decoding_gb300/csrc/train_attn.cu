@@ -15,22 +15,33 @@
 // tiles inside every row's interval take no mask, and the rest take a
 // two-compare interval mask.
 //
-// sm_103a design (one CTA per (batch, head, 128-row query tile)):
-//   warp 0      TMA producer: Q once, then K and V tiles (SW128, 64-column
-//               boxes) into an NS-stage ring with full/empty mbarriers.
-//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T into one of
-//               two 128-column TMEM buffers, O += P V into a D-column TMEM
-//               accumulator; completion is signalled with tcgen05.commit.
-//   warps 2..5  softmax (thread = query row = TMEM lane): S from TMEM, mask,
-//               row max, exp2, P (bf16) into shared memory in the K-major
-//               SW128 layout the PV MMA reads (on partial tiles as a hi + lo
-//               pair of bf16 terms, two PV passes); O in TMEM is rescaled only when
-//               the row max grew by more than 2^8 (lazy rescaling), and the
-//               epilogue normalises O and stores bf16 (and the log-sum-exp).
-// The MMA warp issues S(n) before PV(n-1), so the tensor cores compute the
-// next scores while the softmax warps work on the current ones.
+// sm_103a design.  A work item is one 128-row query tile of one or two query
+// heads that share a KV head (so both read the same K/V tiles); items are
+// taken heaviest first by persistent CTAs (one per SM).
+//   warp 0      TMA producer: the item's Q tiles, then K and V tiles (SW128,
+//               64-column boxes) into an NS-stage ring (full/empty mbarriers).
+//   warp 1      TMEM owner and MMA issuer (one thread).  Per key tile n the
+//               tensor pipe runs, in issue order,
+//                 PV_A(n), S_A(n+1) = Q_A K(n+1)^T, PV_B(n), S_B(n+1),
+//               so while softmax warpgroup A works on S_A the tensor cores
+//               compute B's products, and vice versa.  tcgen05 operations of
+//               one thread execute in order, so S_X(n+1) overwrites the TMEM
+//               columns that PV_X(n) reads only after PV_X(n) has read them,
+//               and the commit after S_X(n+1) also covers PV_X(n).
+//   warps 2..5  softmax warpgroup A, warps 6..9 warpgroup B (thread = query
+//               row = TMEM lane): S from TMEM, mask, row max, exp2; P is
+//               written back over S in TMEM as bf16 pairs and PV reads it
+//               from there (the A operand of tcgen05.mma may live in TMEM).
+//               On the partial tiles of the first query tile of each stream P
+//               is also split into hi + lo bf16 terms (two PV passes): the rows
+//               that see only a few keys, and so have no averaging to hide the
+//               2^-9 rounding of a single bf16 P, all live there (every later
+//               row sees at least ~B * floor(128 / B) keys).  O in TMEM is
+//               rescaled only when the row max grows by more than 2^8 (lazy
+//               rescaling); the epilogue normalises O and stores bf16 and the
+//               log-sum-exp.
 // Every mbarrier wait is bounded; a wait that gives up sets MARS_DEV_TIMEOUT
-// in the status word and the CTA winds down without further waiting.
+// in the status word and the role winds down without further waiting.
 #include <cuda.h>
 
 #include <algorithm>
@@ -42,25 +53,28 @@ namespace {
 
 using namespace mars;
 
-constexpr int kBM = 128;        // query rows per CTA
+constexpr int kBM = 128;        // query rows per query tile
 constexpr int kBN = 128;        // keys per tile
 constexpr int kBox = 128 * 128; // bytes of one [128 rows x 64 bf16] SW128 box
+constexpr int kOBox = 32 * 128; // bytes of one [32 rows x 64 bf16] SW128 output box
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
+// 10 warps: TMA producer (warp 0), MMA issuer (warp 1), softmax warpgroups A
+// (warps 2..5) and B (warps 6..9).  Three warps share some SM sub-partitions,
+// which caps the kernel at 168 registers per thread.
+constexpr int kThreads = 320;
 
 template <int D>
 struct Cfg {
   static constexpr int NB = D / 64;  // 64-column boxes per row block
-  static constexpr int NS = D == 64 ? 3 : 2;
-  static constexpr int Q_BYTES = NB * kBox;
+  static constexpr int NS = D == 64 ? 4 : 2;
+  static constexpr int Q_BYTES = NB * kBox;   // one query tile
   static constexpr int KV_BYTES = NB * kBox;  // one K (or V) tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_BYTES;
+  static constexpr int Q_OFF = 0;             // Q_A, Q_B
+  static constexpr int K_OFF = Q_OFF + 2 * Q_BYTES;
   static constexpr int V_OFF = K_OFF + NS * KV_BYTES;
-  static constexpr int P_OFF = V_OFF + NS * KV_BYTES;
-  static constexpr int P_BYTES = 2 * kBox;
-  static constexpr int PLO_OFF = P_OFF + P_BYTES;       // low bf16 part of P on partial tiles
-  static constexpr int SMEM = PLO_OFF + P_BYTES + 1024;  // + slack to align the base to 1024
-  static constexpr int TMEM_COLS = 512;                 // S0 | S1 | O
+  static constexpr int O_OFF = V_OFF + NS * KV_BYTES;  // per softmax warp: one [32 rows x 64] SW128 box
+  static constexpr int SMEM = O_OFF + 8 * kOBox + 1024;  // + slack to align the base to 1024
+  static constexpr int TMEM_COLS = 512;                      // S_A | S_B | O_A | O_B
   static constexpr int O_COL = 2 * kBN;
 };
 
@@ -70,7 +84,9 @@ struct TrainArgs {
   int32_t* status;
   int batch, L, B, Hq, Hkv, G;
   float scale_log2;
-  int nq;         // query tiles per stream
+  int nq;      // query tiles per stream
+  int pairs;   // head slots per KV group: ceil(G / 2)
+  int items;   // 2 * nq * batch * Hkv * pairs
 };
 
 // SW128 K-major / MN-major shared-memory matrix descriptor (tcgen05 format).
@@ -128,42 +144,60 @@ __device__ __forceinline__ Sched make_sched(bool noisy_q, int j, int L, int B) {
   return s;
 }
 
+// One work item: query tile (noisy_q, j) of heads h_a and (when two_q) h_a + 1
+// of batch b, sharing KV head g.  Items are numbered heaviest query tile first
+// (noisy j, clean j for j = nq-1 .. 0), then batch / KV head / head pair.
+struct Item {
+  int b, g, h_a, j, r0, row_end;
+  bool noisy_q, two_q;
+  Sched sched;
+};
+
+__device__ __forceinline__ Item item_of(const TrainArgs& a, int idx) {
+  Item it;
+  const int per_rank = a.batch * a.Hkv * a.pairs;
+  const int rank = idx / per_rank;
+  int rest = idx % per_rank;
+  const int pair = rest % a.pairs;
+  rest /= a.pairs;
+  it.g = rest % a.Hkv;
+  it.b = rest / a.Hkv;
+  it.h_a = it.g * a.G + 2 * pair;
+  it.two_q = 2 * pair + 1 < a.G;
+  it.j = a.nq - 1 - rank / 2;
+  it.noisy_q = (rank & 1) == 0;
+  it.r0 = it.noisy_q ? a.L + kBM * it.j : kBM * it.j;
+  it.row_end = it.noisy_q ? 2 * a.L : a.L;
+  it.sched = make_sched(it.noisy_q, it.j, a.L, a.B);
+  return it;
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     train_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const TrainArgs a) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const TrainArgs a) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q, bar_k[C::NS], bar_v[C::NS], bar_kv_empty[C::NS], bar_s[2], bar_p,
-      bar_pv;
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_k[C::NS], bar_v[C::NS], bar_kv_empty[C::NS],
+      bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- which query tile: heaviest first (noisy j, clean j for j = nq-1 .. 0), heads innermost
-  const int bh_count = a.batch * a.Hq;
-  const int rank = blockIdx.x / bh_count;
-  const int bh = blockIdx.x % bh_count;
-  const int b = bh / a.Hq, h = bh % a.Hq, g = h / a.G;
-  const int j = a.nq - 1 - rank / 2;
-  const bool noisy_q = (rank & 1) == 0;
-  const int r0 = noisy_q ? a.L + kBM * j : kBM * j;   // first z row of the tile
-  const int row_end = noisy_q ? 2 * a.L : a.L;       // rows at or past this are not stored
-  const Sched sched = make_sched(noisy_q, j, a.L, a.B);
-  const int ntiles = sched.count();
-
   if (threadIdx.x == 0) {
-    mbar_init(&bar_q, 1);
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&bar_k[s], 1);
       mbar_init(&bar_v[s], 1);
       mbar_init(&bar_kv_empty[s], 1);
     }
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_pv, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s[x], 1);
+      mbar_init(&bar_p[x], 128);
+      mbar_init(&bar_o[x], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
@@ -175,8 +209,6 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t q_s = smem_u32(smem + C::Q_OFF);
   const uint32_t k_s = smem_u32(smem + C::K_OFF);
   const uint32_t v_s = smem_u32(smem + C::V_OFF);
-  const uint32_t p_s = smem_u32(smem + C::P_OFF);
-  const uint32_t plo_s = smem_u32(smem + C::PLO_OFF);
 
   if (warp == 0) {
     // ================= TMA producer
@@ -184,23 +216,37 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bar_q, C::Q_BYTES);
-      for (int c = 0; c < C::NB; ++c) tma_load_4d(q_s + c * kBox, &tm_q, &bar_q, 64 * c, h, r0, b);
-      for (int n = 0; n < ntiles; ++n) {
-        const int st = n % C::NS;
-        if (n >= C::NS && !mbar_wait(&bar_kv_empty[st], ((n / C::NS) - 1) & 1)) {
+      int kt = 0, t = 0;  // CTA-local key-tile and item counters
+      for (int idx = blockIdx.x; idx < a.items; idx += gridDim.x, ++t) {
+        const Item it = item_of(a, idx);
+        if (t > 0 && !mbar_wait(&bar_q_empty, (t - 1) & 1)) {
           set_status(a.status, MARS_DEV_TIMEOUT);
           break;
         }
-        int kstart;
-        bool nz, part;
-        sched.at(n, kstart, nz, part);
-        mbar_arrive_expect_tx(&bar_k[st], C::KV_BYTES);
-        for (int c = 0; c < C::NB; ++c)
-          tma_load_4d(k_s + st * C::KV_BYTES + c * kBox, &tm_k, &bar_k[st], 64 * c, g, kstart, b);
-        mbar_arrive_expect_tx(&bar_v[st], C::KV_BYTES);
-        for (int c = 0; c < C::NB; ++c)
-          tma_load_4d(v_s + st * C::KV_BYTES + c * kBox, &tm_v, &bar_v[st], 64 * c, g, kstart, b);
+        mbar_arrive_expect_tx(&bar_q_full, (it.two_q ? 2 : 1) * C::Q_BYTES);
+        for (int c = 0; c < C::NB; ++c) {
+          tma_load_4d(q_s + c * kBox, &tm_q, &bar_q_full, 64 * c, it.h_a, it.r0, it.b);
+          if (it.two_q) tma_load_4d(q_s + C::Q_BYTES + c * kBox, &tm_q, &bar_q_full, 64 * c, it.h_a + 1, it.r0, it.b);
+        }
+        bool ok = true;
+        for (int n = 0; n < it.sched.count(); ++n, ++kt) {
+          const int st = kt % C::NS;
+          if (kt >= C::NS && !mbar_wait(&bar_kv_empty[st], ((kt / C::NS) - 1) & 1)) {
+            set_status(a.status, MARS_DEV_TIMEOUT);
+            ok = false;
+            break;
+          }
+          int kstart;
+          bool nz, part;
+          it.sched.at(n, kstart, nz, part);
+          mbar_arrive_expect_tx(&bar_k[st], C::KV_BYTES);
+          for (int c = 0; c < C::NB; ++c)
+            tma_load_4d(k_s + st * C::KV_BYTES + c * kBox, &tm_k, &bar_k[st], 64 * c, it.g, kstart, it.b);
+          mbar_arrive_expect_tx(&bar_v[st], C::KV_BYTES);
+          for (int c = 0; c < C::NB; ++c)
+            tma_load_4d(v_s + st * C::KV_BYTES + c * kBox, &tm_v, &bar_v[st], 64 * c, it.g, kstart, it.b);
+        }
+        if (!ok) break;
       }
     }
     __syncwarp();
@@ -209,207 +255,260 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t id_pv = idesc_bf16(kBM, D, true);
-      bool ok = mbar_wait(&bar_q, 0);
-      auto issue_pv = [&](int n) {
-        const int st = n % C::NS;
-        ok = ok && mbar_wait(&bar_p, n & 1);
-        ok = ok && mbar_wait(&bar_v[st], (n / C::NS) & 1);
-        if (!ok) return;
-        int kstart;
-        bool nz, part;
-        sched.at(n, kstart, nz, part);
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t ad = smem_desc(p_s + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(v_s + st * C::KV_BYTES + ks * 16 * 128, kBox, 1024);
-          tc_mma_ss(tmem + C::O_COL, ad, bd, id_pv, (n > 0 || ks > 0) ? 1u : 0u);
+      int kt = 0, t = 0;
+      int cp[2] = {0, 0};  // P-ready phases consumed per query tile
+      bool ok = true;
+      // Descriptor start addresses are in 16-byte units (bits 0..13), so stepping
+      // a descriptor by `bytes` adds bytes >> 4 to its low word.
+      const uint64_t desc_q = smem_desc(q_s, 16, 1024), desc_k = smem_desc(k_s, 16, 1024);
+      const uint64_t desc_v = smem_desc(v_s, kBox, 1024);
+      auto issue_qk = [&](int x, int st) {
+        const uint64_t qa = desc_q + ((x * C::Q_BYTES) >> 4);
+        const uint64_t kb = desc_k + ((st * C::KV_BYTES) >> 4);
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
+          tc_mma_ss(tmem + x * kBN, qa + off, kb + off, id_qk, ks > 0 ? 1u : 0u);
         }
-        if (part) {  // second pass with the low bf16 part of P
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            const uint64_t ad = smem_desc(plo_s + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc(v_s + st * C::KV_BYTES + ks * 16 * 128, kBox, 1024);
-            tc_mma_ss(tmem + C::O_COL, ad, bd, id_pv, 1u);
-          }
-        }
-        tc_commit(&bar_pv);
-        tc_commit(&bar_kv_empty[st]);
+        tc_commit(&bar_s[x]);
       };
-      for (int n = 0; ok && n < ntiles; ++n) {
-        const int st = n % C::NS;
-        ok = mbar_wait(&bar_k[st], (n / C::NS) & 1);
+      auto issue_pv = [&](int x, int st, bool first, bool split) {
+        ok = ok && mbar_wait(&bar_p[x], cp[x] & 1);
+        if (!ok) return;
+        ++cp[x];
+        tc_fence_after();
+        const uint32_t s_col = tmem + x * kBN;  // P_hi in columns [0, 64), P_lo in [64, 128)
+        const uint32_t o_col = tmem + C::O_COL + x * D;
+        const uint64_t vb = desc_v + ((st * C::KV_BYTES) >> 4);
+#pragma unroll 1
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          tc_mma_ts(o_col, s_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
+        if (split) {
+#pragma unroll 1
+          for (int ks = 0; ks < kBN / 16; ++ks) tc_mma_ts(o_col, s_col + 64 + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, 1u);
+        }
+      };
+      for (int idx = blockIdx.x; ok && idx < a.items; idx += gridDim.x, ++t) {
+        const Item it = item_of(a, idx);
+        const int nt = it.sched.count();
+        ok = mbar_wait(&bar_q_full, t & 1);
+        if (!ok) break;
+        // prologue: S(0) for both query tiles
+        ok = mbar_wait(&bar_k[kt % C::NS], (kt / C::NS) & 1);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t s_col = (n & 1) * kBN;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t ad = smem_desc(q_s + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(k_s + st * C::KV_BYTES + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024);
-          tc_mma_ss(tmem + s_col, ad, bd, id_qk, ks > 0 ? 1u : 0u);
+        issue_qk(0, kt % C::NS);
+        if (it.two_q) issue_qk(1, kt % C::NS);
+        if (nt == 1) tc_commit(&bar_q_empty);
+        for (int n = 0; ok && n < nt; ++n, ++kt) {
+          const int st = kt % C::NS, st1 = (kt + 1) % C::NS;
+          const bool last = n + 1 == nt;
+          int kstart;
+          bool nz, part;
+          it.sched.at(n, kstart, nz, part);
+          const bool split = part && it.j == 0;  // same rule as the softmax warps
+          ok = mbar_wait(&bar_v[st], (kt / C::NS) & 1);
+          if (!ok) break;
+          issue_pv(0, st, n == 0, split);
+          if (!ok) break;
+          if (last) tc_commit(&bar_o[0]);
+          if (!last) {
+            ok = mbar_wait(&bar_k[st1], ((kt + 1) / C::NS) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(0, st1);
+          }
+          if (it.two_q) {
+            issue_pv(1, st, n == 0, split);
+            if (!ok) break;
+            if (last) tc_commit(&bar_o[1]);
+            if (!last) issue_qk(1, st1);
+          }
+          if (n + 2 == nt) tc_commit(&bar_q_empty);  // the item's last S products are issued
+          tc_commit(&bar_kv_empty[st]);
         }
-        tc_commit(&bar_s[n & 1]);
-        if (n > 0) issue_pv(n - 1);
       }
-      if (ok) issue_pv(ntiles - 1);
       if (!ok) set_status(a.status, MARS_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
-    // ================= softmax / epilogue (warps 2..5, thread = row)
+    // ================= softmax / epilogue: warpgroup x = 0 (warps 2..5) or 1 (warps 6..9)
+    const int x = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int i = r0 + r;  // z position of this row
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    // visible key intervals of this row: clean [c_lo_v, c_hi_v], noisy [n_lo_v, n_hi_v]
-    int c_hi_v, n_lo_v, n_hi_v;
-    if (i < a.L) {
-      c_hi_v = i;
-      n_lo_v = 1;
-      n_hi_v = 0;
-    } else {
-      const int t = i - a.L;
-      const int c = a.B * (t / a.B);
-      c_hi_v = c - 1;
-      n_lo_v = a.L + c;
-      n_hi_v = i;
-    }
-    float m_used = -INFINITY;  // max the current P values are relative to
-    float l = 0.f;
+    const uint32_t s_col = tmem + lane_addr + x * kBN;
+    const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
+    int cs = 0, co = 0;  // S-ready and O-ready phases consumed
     bool ok = true;
-    uint8_t* p_row = smem + C::P_OFF + r * 128;
-    uint8_t* plo_row = smem + C::PLO_OFF + r * 128;
-    const int sw = r & 7;
-
-    for (int n = 0; n < ntiles; ++n) {
-      int kstart;
-      bool nz, part;
-      sched.at(n, kstart, nz, part);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[n & 1], (n >> 1) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 16) {
-        uint32_t (&chunk)[16] = *reinterpret_cast<uint32_t(*)[16]>(&s[c]);
-        tmem_ld16(tmem + lane_addr + (n & 1) * kBN + c, chunk);
-      }
-      tc_wait_ld();
-      // mask and row max on the raw scores (scale > 0 commutes with max)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      if (part) {
-        const int lo = nz ? n_lo_v : 0;
-        const int hi = nz ? n_hi_v : c_hi_v;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int key = kstart + c;
-          const float x = (key >= lo && key <= hi) ? __uint_as_float(s[c]) : -INFINITY;
-          s[c] = __float_as_uint(x);
-          if (c & 1) mx1 = fmaxf(mx1, x);
-          else mx0 = fmaxf(mx0, x);
-        }
+    for (int idx = blockIdx.x; ok && idx < a.items; idx += gridDim.x) {
+      const Item it = item_of(a, idx);
+      if (x == 1 && !it.two_q) continue;
+      const int h = it.h_a + x;
+      const int i = it.r0 + r;  // z position of this row
+      // visible key intervals of this row: clean [0, c_hi_v], noisy [n_lo_v, n_hi_v]
+      int c_hi_v, n_lo_v, n_hi_v;
+      if (i < a.L) {
+        c_hi_v = i;
+        n_lo_v = 1;
+        n_hi_v = 0;
       } else {
+        const int tt = i - a.L;
+        const int c = a.B * (tt / a.B);
+        c_hi_v = c - 1;
+        n_lo_v = a.L + c;
+        n_hi_v = i;
+      }
+      float m_used = -INFINITY;  // max the current P values are relative to
+      float l = 0.f;
+      const int nt = it.sched.count();
+      for (int n = 0; n < nt; ++n) {
+        int kstart;
+        bool nz, part;
+        it.sched.at(n, kstart, nz, part);
+        const bool split = part && it.j == 0;  // rows that see few keys in total live only here
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[x], cs & 1));
+        if (!ok) break;
+        ++cs;
+        tc_fence_after();
+        // visible columns of this row inside the tile: [vlo, vhi] (empty when vlo > vhi)
+        const int vlo = part ? max((nz ? n_lo_v : 0) - kstart, 0) : 0;
+        const int vhi = part ? min((nz ? n_hi_v : c_hi_v) - kstart, kBN - 1) : kBN - 1;
+        uint32_t s[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
+        for (int c = 0; c < kBN; c += 32) {
+          uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[c]);
+          tmem_ld32(s_col + c, chunk);
+        }
+        tc_wait_ld();
+        // hidden scores become -inf (exp2 of them is exactly 0)
+        if (part) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) s[c] = (c >= vlo && c <= vhi) ? s[c] : 0xFF800000u;
+        }
+        // row max (scale > 0 commutes with max)
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN; c += 4) {
           mx0 = fmaxf(mx0, __uint_as_float(s[c]));
           mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
         }
-      }
-      const float tile_max = fmaxf(mx0, mx1) * a.scale_log2;
-      // lazy rescale: keep the old reference max unless the new one is 2^8 larger
-      float alpha = 1.f;
-      const bool grow = tile_max > m_used + kRescaleThreshold;
-      if (grow) {
-        alpha = fast_exp2(m_used - tile_max);  // 0 when m_used is -inf
-        m_used = tile_max;
-      }
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
-      const float neg_mu = -mu;
-      // P = exp2(s * scale_log2 - mu), kept in fp32 until the P buffer is free
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(s[c]), a.scale_log2, neg_mu));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 1]), a.scale_log2, neg_mu));
-        sum0 += p0;
-        sum1 += p1;
-        s[c] = __float_as_uint(p0);
-        s[c + 1] = __float_as_uint(p1);
-      }
-      l = l * alpha + (sum0 + sum1);
-      // PV(n-1) must be done before O is rescaled and before P is overwritten
-      if (n > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_pv, (n - 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {
+        const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
+        // lazy rescale: keep the old reference max unless the new one is 2^8 larger.
+        // PV_x(n-1) is complete here: S_x(n) was issued after it and its commit covers it.
+        float alpha = 1.f;
+        const bool grow = tile_max > m_used + kRescaleThreshold;
+        if (grow) {
+          alpha = fast_exp2(m_used - tile_max);  // 0 when m_used is -inf
+          m_used = tile_max;
+        }
+        if (n > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
           for (int c = 0; c < D; c += 16) {
             uint32_t ov[16];
-            tmem_ld16(tmem + lane_addr + C::O_COL + c, ov);
+            tmem_ld16(o_col + c, ov);
             tc_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st16(tmem + lane_addr + C::O_COL + c, ov);
+            tmem_st16(o_col + c, ov);
           }
-          tc_wait_st();
         }
-      }
-      // P row -> shared memory, K-major SW128: keys 64*sub + 8*cc .. +7 at chunk cc ^ (r & 7).
-      // On partial tiles P is also split as hi + lo (two bf16 terms): rows that see only a
-      // few keys have no averaging to hide the 2^-9 relative rounding of a single bf16 P.
+        const float neg_mu = m_used == -INFINITY ? 0.f : -m_used;
+        // P = exp2(s * scale_log2 - mu) as bf16 pairs over S in TMEM (all of S is in
+        // registers): hi in columns [0, 64); on partial tiles lo = P - hi in [64, 128)
+        float sum0 = 0.f, sum1 = 0.f;
+        if (!split) {
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        const int sub = c >> 3, cc = c & 7;
-        uint32_t hi[4], lo[4];
+          for (int c = 0; c < kBN; c += 32) {
+            uint32_t hi[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = __uint_as_float(s[8 * c + 2 * e]), p1 = __uint_as_float(s[8 * c + 2 * e + 1]);
-          hi[e] = pack_bf16x2(p0, p1);
-          lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e]), a.scale_log2, neg_mu));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e + 1]), a.scale_log2, neg_mu));
+              sum0 += p0;
+              sum1 += p1;
+              hi[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(s_col + (c >> 1), hi);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; c += 16) {
+            uint32_t hi[8], lo[8];
+            if (!__any_sync(0xffffffffu, vlo <= c + 15 && vhi >= c && vlo <= vhi)) {
+              // no row of this warp sees these 16 keys
+#pragma unroll
+              for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0u;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e]), a.scale_log2, neg_mu));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e + 1]), a.scale_log2, neg_mu));
+                sum0 += p0;
+                sum1 += p1;
+                hi[e] = pack_bf16x2(p0, p1);
+                lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
+              }
+            }
+            tmem_st8(s_col + (c >> 1), hi);
+            tmem_st8(s_col + 64 + (c >> 1), lo);
+          }
         }
-        const int off = sub * kBox + ((cc ^ sw) << 4);
-        *reinterpret_cast<uint4*>(p_row + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        if (part) *reinterpret_cast<uint4*>(plo_row + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        l = l * alpha + (sum0 + sum1);
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p[x]);
       }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar_p);
-    }
+      if (!ok) break;
 
-    // ---- epilogue: O / l -> bf16, log-sum-exp
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_pv, (ntiles - 1) & 1));
-    if (ok) {
+      // ---- epilogue: O / l -> bf16, log-sum-exp
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[x], co & 1));
+      if (!ok) break;
+      ++co;
       tc_fence_after();
       const float inv = 1.f / l;
-      const bool store = i < row_end;
-      uint16_t* dst = a.o + ((static_cast<size_t>(b) * 2 * a.L + i) * a.Hq + h) * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        uint32_t ov[16];
-        tmem_ld16(tmem + lane_addr + C::O_COL + c, ov);
+      const bool store = i < it.row_end;
+      // O / l as bf16 -> this warp's [32 rows x 64] SW128 box in shared memory -> TMA
+      // store, one 64-column box at a time.  The store map views O as
+      // [2 * batch, L, Hq, D] so rows past the end of the stream are not written.
+      const uint32_t obox = smem_u32(smem + C::O_OFF) + (x * 4 + quad) * kOBox;
+      const uint32_t orow = obox + lane * 128;
+#pragma unroll 1
+      for (int bx = 0; bx < C::NB; ++bx) {
+        uint32_t ov[64];
+        tmem_ld32(o_col + 64 * bx, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+        tmem_ld32(o_col + 64 * bx + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+        if (lane == 0) bulk_wait_read_all();  // the previous store out of this box has read it
+        __syncwarp();
         tc_wait_ld();
-        if (store) {
-          uint4 w0 = make_uint4(pack_bf16x2(__uint_as_float(ov[0]) * inv, __uint_as_float(ov[1]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv));
-          uint4 w1 = make_uint4(pack_bf16x2(__uint_as_float(ov[8]) * inv, __uint_as_float(ov[9]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[10]) * inv, __uint_as_float(ov[11]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[12]) * inv, __uint_as_float(ov[13]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[14]) * inv, __uint_as_float(ov[15]) * inv));
-          *reinterpret_cast<uint4*>(dst + c) = w0;
-          *reinterpret_cast<uint4*>(dst + c + 8) = w1;
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+          const uint32_t* f = &ov[8 * c16];
+          const uint32_t w0 = pack_bf16x2(__uint_as_float(f[0]) * inv, __uint_as_float(f[1]) * inv);
+          const uint32_t w1 = pack_bf16x2(__uint_as_float(f[2]) * inv, __uint_as_float(f[3]) * inv);
+          const uint32_t w2 = pack_bf16x2(__uint_as_float(f[4]) * inv, __uint_as_float(f[5]) * inv);
+          const uint32_t w3 = pack_bf16x2(__uint_as_float(f[6]) * inv, __uint_as_float(f[7]) * inv);
+          st_shared_v4(orow + ((c16 ^ (lane & 7)) << 4), w0, w1, w2, w3);
+        }
+        fence_async_smem();
+        __syncwarp();
+        const int row0 = it.r0 - (it.noisy_q ? a.L : 0) + 32 * quad;  // first row of the box in its stream
+        if (lane == 0 && row0 < a.L) {
+          tma_store_4d(&tm_o, obox, 64 * bx, h, row0, 2 * it.b + (it.noisy_q ? 1 : 0));
+          bulk_commit_group();
         }
       }
       if (store && a.lse != nullptr)
-        a.lse[(static_cast<size_t>(b) * a.Hq + h) * 2 * a.L + i] = (m_used + __log2f(l)) * 0.6931471805599453f;
-    } else if (lane == 0) {
-      set_status(a.status, MARS_DEV_TIMEOUT);
+        a.lse[(static_cast<size_t>(it.b) * a.Hq + h) * 2 * a.L + i] = (m_used + __log2f(l)) * 0.6931471805599453f;
+      tc_fence_before();
     }
-    tc_fence_before();
+    if (lane == 0) bulk_wait_all();  // output stores complete before the CTA exits
+    if (!ok && lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
   }
 
+  tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -436,15 +535,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [batch, n, H, D] bf16 viewed as a 4-D tensor with 64-column x 128-row SW128 boxes.
-bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch) {
+// [batch, n, H, D] bf16 viewed as a 4-D tensor with 64-column x box_rows SW128 boxes.
+bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n),
                               static_cast<cuuint64_t>(batch)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(n) * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -452,18 +551,18 @@ bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch) {
 }
 
 template <int D>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TrainArgs& a,
-           cudaStream_t stream) {
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           const TrainArgs& a, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(train_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM) !=
-        cudaSuccess)
-      return MARS_ERR_CUDA;
+    const cudaError_t e =
+        cudaFuncSetAttribute(train_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
     configured = true;
   }
-  const long long grid = static_cast<long long>(a.batch) * a.Hq * 2 * a.nq;
-  train_attn_kernel<D><<<static_cast<unsigned>(grid), 192, Cfg<D>::SMEM, stream>>>(tq, tk, tv, a);
-  return cudaGetLastError() == cudaSuccess ? MARS_OK : MARS_ERR_CUDA;
+  const int grid = std::min(a.items, mars_host::num_sms());
+  train_attn_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(tq, tk, tv, to, a);
+  return mars_host::launch_status();
 }
 
 }  // namespace
@@ -485,9 +584,9 @@ extern "C" int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint1
   int rc = mars_host::check_device();
   if (rc != MARS_OK) return rc;
 
-  CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, D, Hq, 2 * L, batch) || !make_map(&tk, k, D, Hkv, 2 * L, batch) ||
-      !make_map(&tv, v, D, Hkv, 2 * L, batch))
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map(&tq, q, D, Hq, 2 * L, batch, kBM) || !make_map(&tk, k, D, Hkv, 2 * L, batch, kBN) ||
+      !make_map(&tv, v, D, Hkv, 2 * L, batch, kBN) || !make_map(&to, o, D, Hq, L, 2 * batch, 32))
     return MARS_ERR_CUDA;
   TrainArgs a;
   a.o = o;
@@ -501,6 +600,8 @@ extern "C" int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint1
   a.G = Hq / Hkv;
   a.scale_log2 = scale * kLog2e;
   a.nq = nq;
+  a.pairs = (a.G + 1) / 2;
+  a.items = 2 * nq * batch * Hkv * a.pairs;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return D == 64 ? launch<64>(tq, tk, tv, a, s) : launch<128>(tq, tk, tv, a, s);
+  return D == 64 ? launch<64>(tq, tk, tv, to, a, s) : launch<128>(tq, tk, tv, to, a, s);
 }
