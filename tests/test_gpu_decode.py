@@ -104,3 +104,22 @@ def test_deterministic_across_calls():
     a = run_decode(q, kn, vn, kc, vc, [2048], 2100, 128 ** -0.5)
     b = run_decode(q, kn, vn, kc, vc, [2048], 2100, 128 ** -0.5)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_cache_beyond_len_holds_nan(D):
+    """What the cache holds at or past cache_len (here NaN) never reaches the output."""
+    batch, B, hq, hkv, cap = 2, 4, 8, 2, 256
+    lens = np.asarray([70, 129], dtype=np.int32)
+    q = rand_bf16((batch, B, hq, D), 1100)
+    kn, vn = rand_bf16((batch, B, hkv, D), 1101), rand_bf16((batch, B, hkv, D), 1102)
+    kc, vc = rand_bf16((batch, hkv, cap, D), 1103), rand_bf16((batch, hkv, cap, D), 1104)
+    for t in (kc, vc):
+        for b in range(batch):
+            t.bits[b, :, lens[b]:, :] = 0x7FC0  # bf16 quiet NaN
+            t.f64[b, :, lens[b]:, :] = np.nan
+    scale = D ** -0.5
+    got = run_decode(q, kn, vn, kc, vc, lens, cap, scale)
+    assert np.all(np.isfinite(got))
+    want = oracle.decode_attn(q.f64, kn.f64, vn.f64, kc.f64, vc.f64, lens, scale)
+    assert max_abs(got, want) <= ATTN_TOL

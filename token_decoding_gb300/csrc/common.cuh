@@ -33,6 +33,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// One lane of the (converged) warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
 }
@@ -128,6 +135,7 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
 // (and leaves the barrier alone) when the poll limit is reached.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
+  if (mbar_test_wait(a, parity)) return true;  // already complete: no suspend
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(a, parity)) return true;
   }

@@ -7,21 +7,35 @@
 // cursor, filled by one forward) and Eq. 2 (noisy intra-block causal case);
 // the authors' MARS blog post, "Inference: a knob, not a mode switch".
 //
-// Design (HBM-bound: every cached K/V byte is read once):
-//   * A work unit is (sequence b, KV head g, chunk of Gc query heads of that
-//     group).  Its query rows are (head, position) pairs, R = Gc * B <= 128,
-//     so one K/V stream serves all heads that share the KV head (GQA).
-//   * A unit is processed by a cluster of C CTAs; CTA rank r takes the r-th
-//     contiguous share of the unit's 64-key tiles (committed keys followed by
-//     this step's B new keys).  Each CTA keeps an online softmax state per
-//     row; at the end the C states are merged through distributed shared
-//     memory, so no split-K workspace ever reaches global memory.
-//   * K/V tiles are streamed with cp.async (16-byte, XOR-swizzled rows) in a
-//     3-stage ring; Q K^T and P V run on bf16 mma.sync with fp32 accumulation,
-//     softmax in the exp2 domain with fp32 state.
+// sm_103a design (HBM-bound: every cached K/V byte is read once).
+//   * A unit is (sequence b, KV head g, chunk of Gc query heads of that group).
+//     Its query rows are (position i, head) pairs, row = i * Gc + head, at most
+//     128, so one K/V stream serves every head that shares the KV head (GQA).
+//     The rows form the M = 128 side of tcgen05.mma; rows past Gc * B are zero.
+//   * A unit is processed by a cluster of C CTAs; CTA rank c takes the c-th
+//     contiguous share of the unit's 64-key cache tiles, and the last rank also
+//     takes the tile of this step's B new keys (N = 16, rows >= B zero).  At
+//     the end the per-row softmax states of all CTAs are merged through
+//     distributed shared memory: no split-K partials reach global memory.
+//   * Inside a CTA the local tiles alternate between two streams A and B, each
+//     with its own S and O in tensor memory and its own online softmax, so the
+//     tensor pipe computes one stream's products while the other's softmax runs:
+//       warp 0      TMA producer: Q once, the new-key tile once, then K and V
+//                   cache tiles (SW128 boxes) into an NS-stage ring;
+//       warp 1      TMEM owner and MMA issuer: S_x = Q K^T (SS), O_x += P_x V
+//                   (TS: P is read from tensor memory);
+//       warps 2..5  softmax of stream A, warps 6..9 of stream B (thread = query
+//                   row = TMEM lane; warps whose 32 rows are all padding idle).
+//   * Cache keys at or past cache_len are masked, and the V rows that hold them
+//     in the last tile are zeroed in shared memory before P V reads them, so
+//     whatever the cache holds there (even NaN) never reaches the output.
 //   * Units are visited longest-cache-first (a rank computed in every CTA from
 //     cache_len), so the long sequences start early and short ones fill in.
+// Every mbarrier wait is bounded; a wait that gives up sets MARS_DEV_TIMEOUT.
+#include <cuda.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -29,18 +43,35 @@ namespace {
 
 using namespace mars;
 
-constexpr int kTileKeys = 64;
-constexpr int kStages = 3;
-constexpr int kMaxRows = 128;
+constexpr int kTileKeys = 64;    // keys per cache tile
+constexpr int kNewKeys = 16;     // N of the new-key tile (B <= 16)
+constexpr int kRows = 128;       // MMA M: query rows of a unit, zero-padded
 constexpr int kMaxCluster = 8;
 constexpr int kSortLimit = 256;  // sequences; above this units are visited in index order
+constexpr int kThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
+
+template <int D>
+struct DCfg {
+  static constexpr int NB = D / 64;                     // 64-column SW128 boxes per row
+  static constexpr int Q_BOX = kRows * 128;             // bytes of one Q box
+  static constexpr int T_BOX = kTileKeys * 128;         // bytes of one K (or V) tile box
+  static constexpr int N_BOX = kNewKeys * 128;          // bytes of one new-key box
+  static constexpr int NS = D == 64 ? 8 : 5;            // ring stages
+  static constexpr int Q_OFF = 0;
+  static constexpr int NK_OFF = Q_OFF + NB * Q_BOX;     // new K boxes, then new V boxes
+  static constexpr int NV_OFF = NK_OFF + NB * N_BOX;
+  static constexpr int RING_OFF = NV_OFF + NB * N_BOX;  // stage s: K boxes then V boxes
+  static constexpr int STAGE = 2 * NB * T_BOX;
+  static constexpr int SMEM = RING_OFF + NS * STAGE + 1024;  // + slack to align the base to 1024
+  static constexpr int TMEM_COLS = D == 64 ? 256 : 512;       // S_A | S_B | O_A | O_B
+  static constexpr int O_COL = 2 * kTileKeys;
+  // end-of-kernel merge state (overlays the ring): acc [2][128][D] f32, m [2][128], l [2][128]
+  static constexpr int MERGE_BYTES = 2 * kRows * D * 4 + 4 * kRows * 4;
+  static_assert(MERGE_BYTES <= NS * STAGE, "merge state must fit in the ring");
+};
 
 struct DecodeArgs {
-  const uint16_t* q;
-  const uint16_t* k_new;
-  const uint16_t* v_new;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
   const int32_t* cache_len;
   uint16_t* o;
   int32_t* status;
@@ -51,40 +82,49 @@ struct DecodeArgs {
   int nhc;           // head chunks per KV head
   int C;             // CTAs per unit (cluster size)
   int sort_units;
+  int box_rows;      // rows of a cache-tile TMA box: min(64, cap)
 };
 
-template <int D>
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  // byte offset of 16-byte chunk `chunk` of row `row` in a [rows x D] bf16 tile
-  return static_cast<uint32_t>(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
+// SW128 shared-memory matrix descriptor (tcgen05 format).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for sm_100-class tensor cores
+  d |= 2ull << 61;  // 128-byte swizzle
+  return d;
 }
 
-template <int D, int NW>
-__global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeArgs a) {
-  constexpr int RP = NW * 16;           // padded rows
-  constexpr int NT = NW * 32;           // threads
-  constexpr int CPR = D / 8;            // 16-byte chunks per row
-  constexpr int KT = D / 16;            // k-steps of Q K^T
-  constexpr int DT = D / 8;             // n-tiles of P V
-  constexpr uint32_t kTileBytes = kTileKeys * D * 2;
+// Instruction descriptor: bf16 x bf16 -> fp32, dense, M x N, A K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* q_s = smem;
-  uint8_t* kv_s = smem + RP * D * 2;  // [stage][K tile | V tile]
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                  const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kn,
+                  const __grid_constant__ CUtensorMap tm_vn, const DecodeArgs a) {
+  using C = DCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_q, bar_new, bar_kv[C::NS], bar_kv_empty[C::NS], bar_s[2], bar_p[2], bar_o[2];
+  __shared__ uint32_t tmem_slot;
   __shared__ int s_b;
   __shared__ int s_len[kSortLimit];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int units_per_b = a.Hkv * a.nhc;
   const int unit_rank = blockIdx.x / a.C;
-  const int crank = a.C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int crank = static_cast<int>(cluster_ctarank());
 
   // ---- which sequence: heavy-first rank order (stable by index) or plain order
   const int b_rank = unit_rank / units_per_b;
   if (a.sort_units) {
-    for (int t = tid; t < a.batch; t += NT) s_len[t] = __ldg(a.cache_len + t);
+    for (int t = tid; t < a.batch; t += kThreads) s_len[t] = __ldg(a.cache_len + t);
     __syncthreads();
-    for (int t = tid; t < a.batch; t += NT) {
+    for (int t = tid; t < a.batch; t += kThreads) {
       const int lt = s_len[t];
       int rank = 0;
       for (int u = 0; u < a.batch; ++u) {
@@ -102,17 +142,17 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeArgs a) {
   const int rem = unit_rank % units_per_b;
   const int g = rem / a.nhc;
   const int hc = rem % a.nhc;
-  const int h0 = g * a.G + hc * a.Gc;                // first query head of this unit
-  const int heads = min(a.Gc, a.G - hc * a.Gc);      // heads in this unit
-  const int R = heads * a.B;                         // real rows
+  const int h0 = g * a.G + hc * a.Gc;            // first query head of this unit
+  const int heads = min(a.Gc, a.G - hc * a.Gc);  // real heads in this unit
+  const int R = a.Gc * a.B;                      // rows loaded (row = i * Gc + head)
 
   const int len = __ldg(a.cache_len + b);
   if (len < 0 || len > a.max_len) {
     // Uniform over the cluster: every CTA of the unit sees the same len and returns here.
     if (crank == 0) {
       if (tid == 0) set_status(a.status, MARS_DEV_LEN_RANGE);
-      for (int e = tid; e < R * CPR; e += NT) {
-        const int r = e / CPR, c = e % CPR;
+      for (int e = tid; e < heads * a.B * (D / 8); e += kThreads) {
+        const int r = e / (D / 8), c = e % (D / 8);
         const int hl = r / a.B, i = r % a.B;
         *reinterpret_cast<uint4*>(a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 8 * c) =
             make_uint4(0, 0, 0, 0);
@@ -120,258 +160,384 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeArgs a) {
     }
     return;
   }
-  const int T = len + a.B;  // keys: committed cache + this step's placeholders
-  const int ntiles = (T + kTileKeys - 1) / kTileKeys;
-  const int t0 = static_cast<int>((static_cast<long long>(ntiles) * crank) / a.C);
-  const int t1 = static_cast<int>((static_cast<long long>(ntiles) * (crank + 1)) / a.C);
+  const int nct = (len + kTileKeys - 1) / kTileKeys;  // cache tiles of the unit
+  const int t0 = static_cast<int>((static_cast<long long>(nct) * crank) / a.C);
+  const int t1 = static_cast<int>((static_cast<long long>(nct) * (crank + 1)) / a.C);
+  const int ncache = t1 - t0;
+  const bool has_new = crank == a.C - 1;
+  const int ntiles = ncache + (has_new ? 1 : 0);  // local tile k: cache tile t0 + k, then the new tile
+  const int act_warps = (R + 31) / 32;             // softmax warps per stream with real rows
 
-  const size_t cache_head = (static_cast<size_t>(b) * a.Hkv + g) * a.cap;  // row index of (b, g, 0)
-
-  // ---- Q tile -> smem (rows beyond R are zero)
-  const uint32_t q_base = smem_u32(q_s);
-  for (int e = tid; e < RP * CPR; e += NT) {
-    const int r = e / CPR, c = e % CPR;
-    const bool valid = r < R;
-    const int hl = valid ? r / a.B : 0, i = valid ? r % a.B : 0;
-    const uint16_t* src = a.q + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 8 * c;
-    cp_async16(q_base + swz<D>(r, c), src, valid);
-  }
-  cp_async_commit();
-
-  const uint32_t kv_base = smem_u32(kv_s);
-  auto load_tile = [&](int tile, int stage) {
-    const uint32_t kb = kv_base + stage * 2 * kTileBytes;
-    const uint32_t vb = kb + kTileBytes;
-    for (int e = tid; e < kTileKeys * CPR; e += NT) {
-      const int r = e / CPR, c = e % CPR;
-      const int key = tile * kTileKeys + r;
-      const uint16_t* ks;
-      const uint16_t* vs;
-      bool valid = true;
-      if (key < len) {
-        ks = a.k_cache + (cache_head + key) * D + 8 * c;
-        vs = a.v_cache + (cache_head + key) * D + 8 * c;
-      } else if (key < T) {
-        const size_t off = ((static_cast<size_t>(b) * a.B + (key - len)) * a.Hkv + g) * D + 8 * c;
-        ks = a.k_new + off;
-        vs = a.v_new + off;
+  // ---- zero the rows the TMA loads never write (Q rows >= R, new-key rows >= B)
+  {
+    const uint32_t base = smem_u32(smem);
+    const int qz = (kRows - R) * 8;       // 16-byte chunks per Q box
+    const int nz = (kNewKeys - a.B) * 8;  // per new-key box
+    for (int e = tid; e < C::NB * (qz + 2 * nz); e += kThreads) {
+      uint32_t addr;
+      if (e < C::NB * qz) {
+        const int bx = e / qz, w = e % qz;
+        addr = base + C::Q_OFF + bx * C::Q_BOX + R * 128 + w * 16;
       } else {
-        ks = a.k_new;
-        vs = a.v_new;
-        valid = false;
+        const int f = e - C::NB * qz;
+        const int bx = f / nz, w = f % nz;  // new K boxes, then new V boxes
+        addr = base + C::NK_OFF + bx * C::N_BOX + a.B * 128 + w * 16;
       }
-      cp_async16(kb + swz<D>(r, c), ks, valid);
-      cp_async16(vb + swz<D>(r, c), vs, valid);
+      st_shared_v4(addr, 0u, 0u, 0u, 0u);
     }
-  };
-
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (t0 + s < t1) load_tile(t0 + s, s);
-    cp_async_commit();
+    fence_async_smem();
   }
-
-  // ---- per-warp state: rows warp*16 + lane/4 (+8)
-  float m_r[2] = {-INFINITY, -INFINITY};
-  float l_r[2] = {0.f, 0.f};
-  float acc[DT][4];
-#pragma unroll
-  for (int n = 0; n < DT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  uint32_t qf[KT][4];
-  const int row0 = warp * 16 + (lane >> 2);
-  const int i_row[2] = {row0 % a.B, (row0 + 8) % a.B};
-
-  cp_async_wait<kStages - 2>();
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_new, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bar_kv[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s[x], 1);
+      mbar_init(&bar_p[x], 32 * act_warps);
+      mbar_init(&bar_o[x], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
   __syncthreads();
-#pragma unroll
-  for (int kk = 0; kk < KT; ++kk) {
-    const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int c = 2 * kk + (lane >> 4);
-    ldsm_x4(q_base + swz<D>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-  }
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
 
-  for (int tile = t0; tile < t1; ++tile) {
-    const int it = tile - t0;
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    {
-      const int nt = tile + kStages - 1;
-      if (nt < t1) load_tile(nt, (it + kStages - 1) % kStages);
-      cp_async_commit();
-    }
-    const uint32_t kb = kv_base + (it % kStages) * 2 * kTileBytes;
-    const uint32_t vb = kb + kTileBytes;
+  const uint32_t q_s = smem_u32(smem + C::Q_OFF);
+  const uint32_t nk_s = smem_u32(smem + C::NK_OFF);
+  const uint32_t nv_s = smem_u32(smem + C::NV_OFF);
+  const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  bool ok = true;
 
-    // S = Q K^T  (16 rows x 64 keys per warp)
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-#pragma unroll
-      for (int j2 = 0; j2 < 4; ++j2) {
-        uint32_t b0, b1, b2, b3;
-        const int r = 16 * j2 + (lane & 7) + (lane >> 4) * 8;
-        const int c = 2 * kk + ((lane >> 3) & 1);
-        ldsm_x4(kb + swz<D>(r, c), b0, b1, b2, b3);
-        mma_bf16_16816(s[2 * j2], qf[kk], b0, b1);
-        mma_bf16_16816(s[2 * j2 + 1], qf[kk], b2, b3);
+  if (warp == 0) {
+    // ================= TMA producer (everything it loads is consumed before the CTA exits)
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kc);
+      tma_prefetch_desc(&tm_vc);
+      mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R);
+      for (int c = 0; c < C::NB; ++c) tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
+      if (has_new) {
+        mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.B);
+        for (int c = 0; c < C::NB; ++c) {
+          tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, b);
+          tma_load_4d(nv_s + c * C::N_BOX, &tm_vn, &bar_new, 64 * c, g, 0, b);
+        }
       }
-    }
-
-    // mask (keys past len + i are invisible) and online softmax in the exp2 domain
-    const int kbase = tile * kTileKeys + 2 * (lane & 3);
-    const bool need_mask = tile * kTileKeys + kTileKeys - 1 > len;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int hr = e >> 1;
-        float x = s[j][e] * a.scale_log2;
-        if (need_mask && kbase + 8 * j + (e & 1) > len + i_row[hr]) x = -INFINITY;
-        s[j][e] = x;
-        mx[hr] = fmaxf(mx[hr], x);
+      const uint32_t tile_bytes = C::NB * 128 * a.box_rows;
+      for (int k = 0; k < ncache; ++k) {
+        const int st = k % C::NS;
+        if (k >= C::NS && !mbar_wait(&bar_kv_empty[st], ((k / C::NS) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int key0 = (t0 + k) * kTileKeys;
+        const uint32_t kb = ring + st * C::STAGE, vb = kb + C::NB * C::T_BOX;
+        mbar_arrive_expect_tx(&bar_kv[st], 2 * tile_bytes);
+        for (int c = 0; c < C::NB; ++c) {
+          tma_load_4d(kb + c * C::T_BOX, &tm_kc, &bar_kv[st], 64 * c, key0, g, b);
+          tma_load_4d(vb + c * C::T_BOX, &tm_vc, &bar_kv[st], 64 * c, key0, g, b);
+        }
       }
+      if (!ok) set_status(a.status, MARS_DEV_TIMEOUT);
     }
-    float alpha[2], mu[2];
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer.  The whole warp runs the schedule, so the
+    // descriptors stay warp-uniform; one elected lane issues the tcgen05
+    // operations and their commits (a commit tracks its own thread's MMAs).
+    if (ntiles > 0) {
+      const bool leader = elect_one();
+      constexpr uint32_t id_qk = idesc_bf16(kRows, kTileKeys, false);
+      constexpr uint32_t id_qn = idesc_bf16(kRows, kNewKeys, false);
+      constexpr uint32_t id_pv = idesc_bf16(kRows, D, true);
+      const uint64_t desc_q = smem_desc(q_s, 16, 1024);
+      const uint64_t desc_nk = smem_desc(nk_s, 16, 1024);
+      const uint64_t desc_nv = smem_desc(nv_s, C::N_BOX, 1024);
+      const uint64_t desc_k = smem_desc(ring, 16, 1024);
+      const uint64_t desc_v = smem_desc(ring + C::NB * C::T_BOX, C::T_BOX, 1024);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_q, 0));
+      // Descriptor start addresses are in 16-byte units, so stepping by `bytes` adds bytes >> 4.
+      auto issue_qk = [&](int k) {
+        const uint32_t d_tmem = tmem + (k & 1) * kTileKeys;
+        const bool cache_tile = k < ncache;
+        const int st = k % C::NS;
+        ok = ok && __all_sync(0xffffffffu, cache_tile ? mbar_wait(&bar_kv[st], (k / C::NS) & 1) : mbar_wait(&bar_new, 0));
+        if (!ok) return;
+        tc_fence_after();
+        if (leader) {
+          if (cache_tile) {
+            const uint64_t kb = desc_k + ((st * C::STAGE) >> 4);
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-      const float mnew = fmaxf(m_r[hr], mx[hr]);
-      mu[hr] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[hr] = fast_exp2(m_r[hr] - mu[hr]);  // exp2(-inf) = 0 on the first visible tile
-      m_r[hr] = mnew;
-      l_r[hr] *= alpha[hr];
-    }
+            for (int ks = 0; ks < D / 16; ++ks)
+              tc_mma_ss(d_tmem, desc_q + (((ks >> 2) * C::Q_BOX + (ks & 3) * 32) >> 4),
+                        kb + (((ks >> 2) * C::T_BOX + (ks & 3) * 32) >> 4), id_qk, ks > 0 ? 1u : 0u);
+          } else {
 #pragma unroll
-    for (int n = 0; n < DT; ++n) {
-      acc[n][0] *= alpha[0];
-      acc[n][1] *= alpha[0];
-      acc[n][2] *= alpha[1];
-      acc[n][3] *= alpha[1];
-    }
-    uint32_t pf[4][4];
+            for (int ks = 0; ks < D / 16; ++ks)
+              tc_mma_ss(d_tmem, desc_q + (((ks >> 2) * C::Q_BOX + (ks & 3) * 32) >> 4),
+                        desc_nk + (((ks >> 2) * C::N_BOX + (ks & 3) * 32) >> 4), id_qn, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&bar_s[k & 1]);
+        }
+        __syncwarp();
+      };
+      auto issue_pv = [&](int k) {
+        const int x = k & 1;
+        const bool cache_tile = k < ncache;
+        const int st = k % C::NS;
+        // K and V of the tile arrived before its S product was issued
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar_p[x], (k >> 1) & 1));
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t p_tmem = tmem + x * kTileKeys;  // P as bf16 pairs in the first 32 columns of S_x
+        const uint32_t o_tmem = tmem + C::O_COL + x * D;
+        const bool first = k < 2;
+        if (leader) {
+          if (cache_tile) {
+            const uint64_t vb = desc_v + ((st * C::STAGE) >> 4);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p0 = fast_exp2(s[j][0] - mu[0]);
-      const float p1 = fast_exp2(s[j][1] - mu[0]);
-      const float p2 = fast_exp2(s[j][2] - mu[1]);
-      const float p3 = fast_exp2(s[j][3] - mu[1]);
-      l_r[0] += p0 + p1;
-      l_r[1] += p2 + p3;
-      // accumulator layout of n-tile j -> A-fragment layout of k-step j/2
-      pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-    }
-
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dn = 0; dn < DT / 2; ++dn) {
-        uint32_t b0, b1, b2, b3;
-        const int r = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = 2 * dn + (lane >> 4);
-        ldsm_x4_t(vb + swz<D>(r, c), b0, b1, b2, b3);
-        mma_bf16_16816(acc[2 * dn], pf[kk], b0, b1);
-        mma_bf16_16816(acc[2 * dn + 1], pf[kk], b2, b3);
+            for (int ks = 0; ks < kTileKeys / 16; ++ks)
+              tc_mma_ts(o_tmem, p_tmem + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
+            tc_commit(&bar_kv_empty[st]);
+          } else {
+            tc_mma_ts(o_tmem, p_tmem, desc_nv, id_pv, first ? 0u : 1u);
+          }
+          if (k + 2 >= ntiles) tc_commit(&bar_o[x]);  // the stream's last product
+        }
+        __syncwarp();
+      };
+      if (ok) issue_qk(0);
+      if (ok && ntiles > 1) issue_qk(1);
+      // S_x(k+2) is issued after O_x += P_x(k) V(k): when S_x(k+2) is complete, so is
+      // every earlier product of stream x, which the softmax relies on to rescale O_x.
+      for (int k = 0; ok && k < ntiles; ++k) {
+        issue_pv(k);
+        if (ok && k + 2 < ntiles) issue_qk(k + 2);
       }
+      if (!ok && leader) set_status(a.status, MARS_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax of stream x (warps 2..5: A, 6..9: B)
+    const int x = (warp - 2) >> 2;
+    const int quad = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = quad * 32 + lane;
+    const bool active = quad < act_warps;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_col = tmem + lane_addr + x * kTileKeys;
+    const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
+    const int pos = r / a.Gc;  // query position i of this row (rows >= R are padding)
+    float m_used = -INFINITY, l = 0.f;
+    int nmine = 0;
+    if (active) {
+      for (int k = x; k < ntiles; k += 2, ++nmine) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[x], nmine & 1));
+        if (!ok) break;
+        tc_fence_after();
+        // last visible column of this tile for this row
+        const bool is_new = k >= ncache;
+        const int key0 = (t0 + k) * kTileKeys;
+        const int vlast = is_new ? pos : len - 1 - key0;
+        uint32_t s[kTileKeys];
+        tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tc_wait_ld();
+        if (is_new || vlast < kTileKeys - 1) {
+#pragma unroll
+          for (int c = 0; c < kTileKeys; ++c) s[c] = c <= vlast ? s[c] : 0xFF800000u;  // -inf
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTileKeys; c += 2) {
+          mx0 = fmaxf(mx0, __uint_as_float(s[c]));
+          mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+        }
+        const float tile_max = fmaxf(mx0, mx1) * a.scale_log2;
+        // lazy rescale: keep the old reference max unless the new one is 2^8 larger
+        float alpha = 1.f;
+        const bool grow = tile_max > m_used + kRescaleThreshold;
+        if (grow) {
+          alpha = fast_exp2(m_used - tile_max);  // 0 when m_used is -inf
+          m_used = tile_max;
+        }
+        if (nmine > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+          for (int c = 0; c < D; c += 16) {
+            uint32_t ov[16];
+            tmem_ld16(o_col + c, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st16(o_col + c, ov);
+          }
+        }
+        const float neg_mu = m_used == -INFINITY ? 0.f : -m_used;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kTileKeys; c += 32) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e]), a.scale_log2, neg_mu));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e + 1]), a.scale_log2, neg_mu));
+            sum0 += p0;
+            sum1 += p1;
+            pw[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_col + (c >> 1), pw);
+        }
+        l = l * alpha + (sum0 + sum1);
+        // The last cache tile can hold keys at or past cache_len: zero those V rows
+        // (whole 128-byte rows of every box) so that P = 0 meets finite values.
+        if (!is_new && len - key0 < kTileKeys) {
+          const int st = k % C::NS;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_kv[st], (k / C::NS) & 1));
+          if (!ok) break;
+          const int z0 = len - key0;
+          const int per_box = (kTileKeys - z0) * 8;  // 16-byte chunks
+          const uint32_t vb = ring + st * C::STAGE + C::NB * C::T_BOX;
+          for (int e = quad * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
+            const int bx = e / per_box, w = e % per_box;
+            st_shared_v4(vb + bx * C::T_BOX + z0 * 128 + w * 16, 0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p[x]);
+      }
+      if (ok && nmine > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[x], 0));
+      if (!ok && lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+    }
+    // Both streams' products are complete once every softmax warp is past its
+    // wait above, so the ring (every loaded tile consumed) can hold the merge state.
+    named_bar_sync(1, 256);
+    tc_fence_after();
+    float* acc_s = reinterpret_cast<float*>(smem + C::RING_OFF);  // [2][128][D], 16-byte units XOR (row & 7)
+    float* m_s = acc_s + 2 * kRows * D;                           // [2][128]
+    float* l_s = m_s + 2 * kRows;                                 // [2][128]
+    if (active) {
+      float4* dst = reinterpret_cast<float4*>(acc_s + (x * kRows + r) * D);
+      const bool have = ok && nmine > 0;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(o_col + c, ov);
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                              __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          dst[((c >> 2) + e) ^ (r & 7)] = v;
+        }
+      }
+      m_s[x * kRows + r] = have ? m_used : -INFINITY;
+      l_s[x * kRows + r] = have ? l : 0.f;
     }
   }
-  cp_async_wait<0>();
 
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
-    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
-  }
-
-  const int col0 = 2 * (lane & 3);
-  if (a.C == 1) {
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = row0 + 8 * hr;
-      if (r >= R) continue;
-      const float inv = 1.f / l_r[hr];
-      const int hl = r / a.B, i = r % a.B;
-      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D;
-#pragma unroll
-      for (int n = 0; n < DT; ++n)
-        *reinterpret_cast<uint32_t*>(dst + 8 * n + col0) = pack_bf16x2(acc[n][2 * hr] * inv, acc[n][2 * hr + 1] * inv);
-    }
-    return;
-  }
-
-  // ---- cluster merge through distributed shared memory
-  __syncthreads();  // every warp is done with the K/V ring, which now holds the states
-  float* acc_s = reinterpret_cast<float*>(kv_s);  // [RP][D]
-  float* m_s = acc_s + RP * D;                     // [RP]
-  float* l_s = m_s + RP;                           // [RP]
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int r = row0 + 8 * hr;
-#pragma unroll
-    for (int n = 0; n < DT; ++n) {
-      acc_s[r * D + 8 * n + col0] = acc[n][2 * hr];
-      acc_s[r * D + 8 * n + col0 + 1] = acc[n][2 * hr + 1];
-    }
-    if ((lane & 3) == 0) {
-      m_s[r] = m_r[hr];
-      l_s[r] = l_r[hr];
-    }
-  }
+  // ---- merge the 2 * C states of every row through distributed shared memory
+  tc_fence_before();
   cluster_sync();
-  const uint32_t acc_local = smem_u32(acc_s), m_local = smem_u32(m_s), l_local = smem_u32(l_s);
-  const int rows_per = (R + a.C - 1) / a.C;
-  const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
-  for (int e = tid; e < (r_hi - r_lo) * (D / 4); e += NT) {
-    const int r = r_lo + e / (D / 4);
-    const int d4 = e % (D / 4);
-    float mmax = -INFINITY;
-    for (int c = 0; c < a.C; ++c) mmax = fmaxf(mmax, dsmem_ld_f32(dsmem_map(m_local + 4 * r, c)));
-    float l = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < a.C; ++c) {
-      const float mc = dsmem_ld_f32(dsmem_map(m_local + 4 * r, c));
-      const float w = mc == -INFINITY ? 0.f : fast_exp2(mc - mmax);
-      l += w * dsmem_ld_f32(dsmem_map(l_local + 4 * r, c));
-      const float4 x = dsmem_ld_f32x4(dsmem_map(acc_local + 4 * (r * D + 4 * d4), c));
-      o.x += w * x.x;
-      o.y += w * x.y;
-      o.z += w * x.z;
-      o.w += w * x.w;
+  {
+    const float* acc_s = reinterpret_cast<const float*>(smem + C::RING_OFF);
+    const float* m_s = acc_s + 2 * kRows * D;
+    const float* l_s = m_s + 2 * kRows;
+    const uint32_t acc_l = smem_u32(acc_s), m_l = smem_u32(m_s), l_l = smem_u32(l_s);
+    const int rows_per = (R + a.C - 1) / a.C;
+    const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
+    for (int e = tid; e < (r_hi - r_lo) * (D / 4); e += kThreads) {
+      const int r = r_lo + e / (D / 4);
+      const int d4 = e % (D / 4);
+      const int i = r / a.Gc, hl = r % a.Gc;
+      if (hl >= heads) continue;
+      float mmax = -INFINITY;
+      for (int c = 0; c < a.C; ++c)
+        for (int x = 0; x < 2; ++x) mmax = fmaxf(mmax, dsmem_ld_f32(dsmem_map(m_l + 4 * (x * kRows + r), c)));
+      float lsum = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < a.C; ++c) {
+        for (int x = 0; x < 2; ++x) {
+          const float mc = dsmem_ld_f32(dsmem_map(m_l + 4 * (x * kRows + r), c));
+          const float w = mc == -INFINITY ? 0.f : fast_exp2(mc - mmax);
+          lsum += w * dsmem_ld_f32(dsmem_map(l_l + 4 * (x * kRows + r), c));
+          const float4 v = dsmem_ld_f32x4(dsmem_map(acc_l + 4 * ((x * kRows + r) * D + 4 * (d4 ^ (r & 7))), c));
+          o.x += w * v.x;
+          o.y += w * v.y;
+          o.z += w * v.z;
+          o.w += w * v.w;
+        }
+      }
+      const float inv = 1.f / lsum;
+      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 4 * d4;
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
     }
-    const float inv = 1.f / l;
-    const int hl = r / a.B, i = r % a.B;
-    uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 4 * d4;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
   }
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
 }
 
-template <int D, int NW>
-size_t smem_bytes() {
-  const size_t ring = static_cast<size_t>(kStages) * 2 * kTileKeys * D * 2;
-  const size_t merge = static_cast<size_t>(NW * 16) * D * 4 + 2 * NW * 16 * 4;
-  return static_cast<size_t>(NW * 16) * D * 2 + std::max(ring, merge);
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
 }
 
-template <int D, int NW>
-int launch(const DecodeArgs& a, int units, cudaStream_t stream) {
-  auto kern = decode_kernel<D, NW>;
-  const size_t smem = smem_bytes<D, NW>();
+// A contiguous bf16 tensor with dims d[0] (innermost, = D) .. d[3], loaded in
+// SW128 boxes of 64 x box1 x box2 x 1 elements.
+bool make_map(CUtensorMap* m, const void* ptr, const long long (&d)[4], int box1, int box2) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d[0]), static_cast<cuuint64_t>(d[1]),
+                              static_cast<cuuint64_t>(d[2]), static_cast<cuuint64_t>(d[3])};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d[0]) * 2, static_cast<cuuint64_t>(d[0] * d[1]) * 2,
+                                 static_cast<cuuint64_t>(d[0] * d[1] * d[2]) * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Maps {
+  CUtensorMap q, kc, vc, kn, vn;
+};
+
+template <int D>
+int launch(const Maps& mp, const DecodeArgs& a, int units, cudaStream_t stream) {
+  auto kern = decode_kernel<D>;
   static bool configured = false;  // per instantiation; the attribute is process-wide
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units * a.C, 1, 1);
-  cfg.blockDim = dim3(NW * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = DCfg<D>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -380,17 +546,9 @@ int launch(const DecodeArgs& a, int units, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.q, mp.kc, mp.vc, mp.kn, mp.vn, a);
   if (e != cudaSuccess) return mars_host::cuda_fail(e);
   return MARS_OK;
-}
-
-template <int D>
-int dispatch_rows(const DecodeArgs& a, int units, int rows, cudaStream_t s) {
-  if (rows <= 16) return launch<D, 1>(a, units, s);
-  if (rows <= 32) return launch<D, 2>(a, units, s);
-  if (rows <= 64) return launch<D, 4>(a, units, s);
-  return launch<D, 8>(a, units, s);
 }
 
 inline int ceil_div(long long x, long long y) { return static_cast<int>((x + y - 1) / y); }
@@ -419,11 +577,6 @@ extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const 
   if (rc != MARS_OK) return rc;
 
   DecodeArgs a;
-  a.q = q;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
   a.cache_len = cache_len;
   a.o = o;
   a.status = status;
@@ -435,29 +588,28 @@ extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const 
   a.max_len = max_len;
   a.scale_log2 = scale * kLog2e;
   a.G = Hq / Hkv;
-
-  // Heads per unit: as many as fit in 128 rows, fewer when that leaves the GPU idle.
-  const int sms = mars_host::num_sms();
-  int Gc = std::min(a.G, kMaxRows / B);
-  int nhc = ceil_div(a.G, Gc);
-  const long long base_units = static_cast<long long>(batch) * Hkv;
-  while (Gc > 1 && base_units * nhc * kMaxCluster < sms) {
-    Gc = ceil_div(Gc, 2);
-    nhc = ceil_div(a.G, Gc);
-  }
-  const long long units = base_units * nhc;
+  // Heads per unit: as many as fit in the 128 rows of one MMA tile.
+  a.Gc = std::min(a.G, kRows / B);
+  a.nhc = ceil_div(a.G, a.Gc);
+  const long long units = static_cast<long long>(batch) * Hkv * a.nhc;
   MARS_HOST_CHECK(units * kMaxCluster < (1LL << 31), MARS_ERR_INVALID_ARG);
-  const int max_tiles = ceil_div(static_cast<long long>(max_len) + B, kTileKeys);
-  int C = pow2_ceil(std::max(1, ceil_div(2LL * sms, units)));
-  C = std::min(C, kMaxCluster);
-  while (C > 1 && C > max_tiles) C >>= 1;
-  a.Gc = Gc;
-  a.nhc = nhc;
-  a.C = C;
+  // CTAs per unit: about two per SM over the whole grid, at most one per cache
+  // tile of the longest sequence.
+  const int sms = mars_host::num_sms();
+  const int max_tiles = std::max(1, ceil_div(max_len, kTileKeys));
+  int cl = pow2_ceil(std::max(1, ceil_div(2LL * sms, units)));
+  cl = std::min(cl, kMaxCluster);
+  while (cl > 1 && cl > max_tiles) cl >>= 1;
+  a.C = cl;
   a.sort_units = (batch > 1 && batch <= kSortLimit) ? 1 : 0;
+  a.box_rows = std::min(cap, kTileKeys);
 
-  const int rows = Gc * B;
+  Maps mp;
+  const long long dq[4] = {D, Hq, B, batch}, dc[4] = {D, cap, Hkv, batch}, dn[4] = {D, Hkv, B, batch};
+  if (!make_map(&mp.q, q, dq, a.Gc, B) || !make_map(&mp.kc, k_cache, dc, a.box_rows, 1) ||
+      !make_map(&mp.vc, v_cache, dc, a.box_rows, 1) || !make_map(&mp.kn, k_new, dn, 1, B) ||
+      !make_map(&mp.vn, v_new, dn, 1, B))
+    return MARS_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return D == 64 ? dispatch_rows<64>(a, static_cast<int>(units), rows, s)
-                 : dispatch_rows<128>(a, static_cast<int>(units), rows, s);
+  return D == 64 ? launch<64>(mp, a, static_cast<int>(units), s) : launch<128>(mp, a, static_cast<int>(units), s);
 }

@@ -251,8 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ================= MMA issuer
-    if (lane == 0) {
+    // ================= MMA issuer.  The whole warp runs the schedule, so the
+    // descriptors stay warp-uniform; one elected lane issues the tcgen05
+    // operations and their commits (a commit tracks its own thread's MMAs).
+    {
+      const bool leader = elect_one();
       constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t id_pv = idesc_bf16(kBM, D, true);
       int kt = 0, t = 0;
@@ -262,44 +265,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a descriptor by `bytes` adds bytes >> 4 to its low word.
       const uint64_t desc_q = smem_desc(q_s, 16, 1024), desc_k = smem_desc(k_s, 16, 1024);
       const uint64_t desc_v = smem_desc(v_s, kBox, 1024);
+      auto wait_all = [&](uint64_t* bar, int parity) {
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity));
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (leader) tc_commit(bar);
+      };
       auto issue_qk = [&](int x, int st) {
         const uint64_t qa = desc_q + ((x * C::Q_BYTES) >> 4);
         const uint64_t kb = desc_k + ((st * C::KV_BYTES) >> 4);
-#pragma unroll 1
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
-          tc_mma_ss(tmem + x * kBN, qa + off, kb + off, id_qk, ks > 0 ? 1u : 0u);
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
+            tc_mma_ss(tmem + x * kBN, qa + off, kb + off, id_qk, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&bar_s[x]);
         }
-        tc_commit(&bar_s[x]);
+        __syncwarp();
       };
       auto issue_pv = [&](int x, int st, bool first, bool split) {
-        ok = ok && mbar_wait(&bar_p[x], cp[x] & 1);
+        wait_all(&bar_p[x], cp[x] & 1);
         if (!ok) return;
         ++cp[x];
         tc_fence_after();
         const uint32_t s_col = tmem + x * kBN;  // P_hi in columns [0, 64), P_lo in [64, 128)
         const uint32_t o_col = tmem + C::O_COL + x * D;
         const uint64_t vb = desc_v + ((st * C::KV_BYTES) >> 4);
-#pragma unroll 1
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          tc_mma_ts(o_col, s_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
-        if (split) {
-#pragma unroll 1
-          for (int ks = 0; ks < kBN / 16; ++ks) tc_mma_ts(o_col, s_col + 64 + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, 1u);
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            tc_mma_ts(o_col, s_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
+          if (split) {
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              tc_mma_ts(o_col, s_col + 64 + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, 1u);
+          }
         }
+        __syncwarp();
       };
       for (int idx = blockIdx.x; ok && idx < a.items; idx += gridDim.x, ++t) {
         const Item it = item_of(a, idx);
         const int nt = it.sched.count();
-        ok = mbar_wait(&bar_q_full, t & 1);
-        if (!ok) break;
+        wait_all(&bar_q_full, t & 1);
         // prologue: S(0) for both query tiles
-        ok = mbar_wait(&bar_k[kt % C::NS], (kt / C::NS) & 1);
+        wait_all(&bar_k[kt % C::NS], (kt / C::NS) & 1);
         if (!ok) break;
         tc_fence_after();
         issue_qk(0, kt % C::NS);
         if (it.two_q) issue_qk(1, kt % C::NS);
-        if (nt == 1) tc_commit(&bar_q_empty);
+        if (nt == 1) commit(&bar_q_empty);
         for (int n = 0; ok && n < nt; ++n, ++kt) {
           const int st = kt % C::NS, st1 = (kt + 1) % C::NS;
           const bool last = n + 1 == nt;
@@ -307,13 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool nz, part;
           it.sched.at(n, kstart, nz, part);
           const bool split = part && it.j == 0;  // same rule as the softmax warps
-          ok = mbar_wait(&bar_v[st], (kt / C::NS) & 1);
+          wait_all(&bar_v[st], (kt / C::NS) & 1);
           if (!ok) break;
           issue_pv(0, st, n == 0, split);
           if (!ok) break;
-          if (last) tc_commit(&bar_o[0]);
+          if (last) commit(&bar_o[0]);
           if (!last) {
-            ok = mbar_wait(&bar_k[st1], ((kt + 1) / C::NS) & 1);
+            wait_all(&bar_k[st1], ((kt + 1) / C::NS) & 1);
             if (!ok) break;
             tc_fence_after();
             issue_qk(0, st1);
@@ -321,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it.two_q) {
             issue_pv(1, st, n == 0, split);
             if (!ok) break;
-            if (last) tc_commit(&bar_o[1]);
+            if (last) commit(&bar_o[1]);
             if (!last) issue_qk(1, st1);
           }
-          if (n + 2 == nt) tc_commit(&bar_q_empty);  // the item's last S products are issued
-          tc_commit(&bar_kv_empty[st]);
+          if (n + 2 == nt) commit(&bar_q_empty);  // the item's last S products are issued
+          commit(&bar_kv_empty[st]);
         }
       }
-      if (!ok) set_status(a.status, MARS_DEV_TIMEOUT);
+      if (!ok && leader) set_status(a.status, MARS_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
