@@ -66,8 +66,9 @@ struct DCfg {
   static constexpr int SMEM = RING_OFF + NS * STAGE + 1024;  // + slack to align the base to 1024
   static constexpr int TMEM_COLS = D == 64 ? 256 : 512;       // S_A | S_B | O_A | O_B
   static constexpr int O_COL = 2 * kTileKeys;
-  // end-of-kernel merge state (overlays the ring): acc [2][128][D] f32, m [2][128], l [2][128]
-  static constexpr int MERGE_BYTES = 2 * kRows * D * 4 + 4 * kRows * 4;
+  // end-of-kernel merge state (overlays the ring): acc [2][128][D] f32, m [2][128], l [2][128],
+  // then this CTA's merge weights [128][2 * kMaxCluster]
+  static constexpr int MERGE_BYTES = 2 * kRows * D * 4 + 4 * kRows * 4 + kRows * 2 * kMaxCluster * 4;
   static_assert(MERGE_BYTES <= NS * STAGE, "merge state must fit in the ring");
 };
 
@@ -119,19 +120,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_rank = blockIdx.x / a.C;
   const int crank = static_cast<int>(cluster_ctarank());
 
+  const int R = a.Gc * a.B;            // rows loaded (row = i * Gc + head)
+  const int act_warps = (R + 31) / 32;  // softmax warps per stream with real rows
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_new, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bar_kv[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s[x], 1);
+      mbar_init(&bar_p[x], 32 * act_warps);
+      mbar_init(&bar_o[x], 1);
+    }
+    fence_mbar_init();
+  }
+
   // ---- which sequence: heavy-first rank order (stable by index) or plain order
   const int b_rank = unit_rank / units_per_b;
   if (a.sort_units) {
     for (int t = tid; t < a.batch; t += kThreads) s_len[t] = __ldg(a.cache_len + t);
     __syncthreads();
-    for (int t = tid; t < a.batch; t += kThreads) {
+    // rank(t) = #{u : len_u > len_t, or len_u == len_t and u < t}, 32 u at a time per warp
+    for (int t = warp; t < a.batch; t += kThreads / 32) {
       const int lt = s_len[t];
       int rank = 0;
-      for (int u = 0; u < a.batch; ++u) {
-        const int lu = s_len[u];
-        rank += (lu > lt) || (lu == lt && u < t);
+      for (int u0 = 0; u0 < a.batch; u0 += 32) {
+        const int u = u0 + lane;
+        const int lu = u < a.batch ? s_len[u] : -1;
+        rank += __popc(__ballot_sync(0xffffffffu, u < a.batch && (lu > lt || (lu == lt && u < t))));
       }
-      if (rank == b_rank) s_b = t;
+      if (lane == 0 && rank == b_rank) s_b = t;
     }
     __syncthreads();
   } else {
@@ -144,9 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hc = rem % a.nhc;
   const int h0 = g * a.G + hc * a.Gc;            // first query head of this unit
   const int heads = min(a.Gc, a.G - hc * a.Gc);  // real heads in this unit
-  const int R = a.Gc * a.B;                      // rows loaded (row = i * Gc + head)
 
-  const int len = __ldg(a.cache_len + b);
+  const int len = a.sort_units ? s_len[b] : __ldg(a.cache_len + b);
   if (len < 0 || len > a.max_len) {
     // Uniform over the cluster: every CTA of the unit sees the same len and returns here.
     if (crank == 0) {
@@ -166,84 +185,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ncache = t1 - t0;
   const bool has_new = crank == a.C - 1;
   const int ntiles = ncache + (has_new ? 1 : 0);  // local tile k: cache tile t0 + k, then the new tile
-  const int act_warps = (R + 31) / 32;             // softmax warps per stream with real rows
-
-  // ---- zero the rows the TMA loads never write (Q rows >= R, new-key rows >= B)
-  {
-    const uint32_t base = smem_u32(smem);
-    const int qz = (kRows - R) * 8;       // 16-byte chunks per Q box
-    const int nz = (kNewKeys - a.B) * 8;  // per new-key box
-    for (int e = tid; e < C::NB * (qz + 2 * nz); e += kThreads) {
-      uint32_t addr;
-      if (e < C::NB * qz) {
-        const int bx = e / qz, w = e % qz;
-        addr = base + C::Q_OFF + bx * C::Q_BOX + R * 128 + w * 16;
-      } else {
-        const int f = e - C::NB * qz;
-        const int bx = f / nz, w = f % nz;  // new K boxes, then new V boxes
-        addr = base + C::NK_OFF + bx * C::N_BOX + a.B * 128 + w * 16;
-      }
-      st_shared_v4(addr, 0u, 0u, 0u, 0u);
-    }
-    fence_async_smem();
-  }
-  if (tid == 0) {
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_new, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&bar_kv[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bar_s[x], 1);
-      mbar_init(&bar_p[x], 32 * act_warps);
-      mbar_init(&bar_o[x], 1);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_slot;
 
   const uint32_t q_s = smem_u32(smem + C::Q_OFF);
   const uint32_t nk_s = smem_u32(smem + C::NK_OFF);
   const uint32_t nv_s = smem_u32(smem + C::NV_OFF);
   const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  const uint32_t tile_bytes = C::NB * 128 * a.box_rows;
+  // TMA loads of cache tile k into its ring stage (the stage is free)
+  auto load_tile = [&](int k) {
+    const int st = k % C::NS;
+    const int key0 = (t0 + k) * kTileKeys;
+    const uint32_t kb = ring + st * C::STAGE, vb = kb + C::NB * C::T_BOX;
+    mbar_arrive_expect_tx(&bar_kv[st], 2 * tile_bytes);
+    for (int c = 0; c < C::NB; ++c) {
+      tma_load_4d(kb + c * C::T_BOX, &tm_kc, &bar_kv[st], 64 * c, key0, g, b);
+      tma_load_4d(vb + c * C::T_BOX, &tm_vc, &bar_kv[st], 64 * c, key0, g, b);
+    }
+  };
+  // The producer thread starts the loads before the rest of the set-up: they write
+  // rows the zeroing below never touches.
+  if (tid == 0 && ntiles > 0) {
+    mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R);
+    for (int c = 0; c < C::NB; ++c) tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
+    for (int k = 0; k < min(ncache, C::NS); ++k) load_tile(k);
+    if (has_new) {
+      mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.B);
+      for (int c = 0; c < C::NB; ++c) {
+        tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, b);
+        tma_load_4d(nv_s + c * C::N_BOX, &tm_vn, &bar_new, 64 * c, g, 0, b);
+      }
+    }
+  }
+
+  // ---- zero the rows the TMA loads never write (Q rows >= R, new-key rows >= B):
+  // the tail of every Q box and of every new-key box
+  for (int bx = 0; bx < C::NB; ++bx)
+    for (int e = tid; e < (kRows - R) * 8; e += kThreads) st_shared_v4(q_s + bx * C::Q_BOX + R * 128 + e * 16, 0u, 0u, 0u, 0u);
+  for (int bx = 0; bx < 2 * C::NB; ++bx)  // new K boxes, then new V boxes
+    for (int e = tid; e < (kNewKeys - a.B) * 8; e += kThreads)
+      st_shared_v4(nk_s + bx * C::N_BOX + a.B * 128 + e * 16, 0u, 0u, 0u, 0u);
+  fence_async_smem();
+  if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
   bool ok = true;
 
   if (warp == 0) {
-    // ================= TMA producer (everything it loads is consumed before the CTA exits)
-    if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kc);
-      tma_prefetch_desc(&tm_vc);
-      mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R);
-      for (int c = 0; c < C::NB; ++c) tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
-      if (has_new) {
-        mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.B);
-        for (int c = 0; c < C::NB; ++c) {
-          tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, b);
-          tma_load_4d(nv_s + c * C::N_BOX, &tm_vn, &bar_new, 64 * c, g, 0, b);
-        }
-      }
-      const uint32_t tile_bytes = C::NB * 128 * a.box_rows;
-      for (int k = 0; k < ncache; ++k) {
-        const int st = k % C::NS;
-        if (k >= C::NS && !mbar_wait(&bar_kv_empty[st], ((k / C::NS) - 1) & 1)) {
-          ok = false;
+    // ================= TMA producer: the tiles past the first NS, each into a freed stage
+    // (everything it loads is consumed before the CTA exits)
+    if (lane == 0) {
+      for (int k = C::NS; k < ncache; ++k) {
+        if (!mbar_wait(&bar_kv_empty[k % C::NS], ((k / C::NS) - 1) & 1)) {
+          set_status(a.status, MARS_DEV_TIMEOUT);
           break;
         }
-        const int key0 = (t0 + k) * kTileKeys;
-        const uint32_t kb = ring + st * C::STAGE, vb = kb + C::NB * C::T_BOX;
-        mbar_arrive_expect_tx(&bar_kv[st], 2 * tile_bytes);
-        for (int c = 0; c < C::NB; ++c) {
-          tma_load_4d(kb + c * C::T_BOX, &tm_kc, &bar_kv[st], 64 * c, key0, g, b);
-          tma_load_4d(vb + c * C::T_BOX, &tm_vc, &bar_kv[st], 64 * c, key0, g, b);
-        }
+        load_tile(k);
       }
-      if (!ok) set_status(a.status, MARS_DEV_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -442,41 +441,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- merge the 2 * C states of every row through distributed shared memory
+  // ---- merge the 2 * C states of every row through distributed shared memory.
+  // This CTA finishes rows [r_lo, r_hi): first one weight per (row, state),
+  // w = 2^(m - max m) / sum_states(2^(m - max m) l), then O = sum w acc.
   tc_fence_before();
   cluster_sync();
   {
     const float* acc_s = reinterpret_cast<const float*>(smem + C::RING_OFF);
     const float* m_s = acc_s + 2 * kRows * D;
     const float* l_s = m_s + 2 * kRows;
+    float* w_s = const_cast<float*>(l_s) + 2 * kRows;  // [rows_per][2 * kMaxCluster], this CTA's own
     const uint32_t acc_l = smem_u32(acc_s), m_l = smem_u32(m_s), l_l = smem_u32(l_s);
     const int rows_per = (R + a.C - 1) / a.C;
     const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
+    const int ns = 2 * a.C;  // states per row
+    for (int r = r_lo + tid; r < r_hi; r += kThreads) {
+      float m[2 * kMaxCluster], l[2 * kMaxCluster];
+      float mmax = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 2 * kMaxCluster; ++q) {
+        if (q < ns) {
+          m[q] = dsmem_ld_f32(dsmem_map(m_l + 4 * ((q & 1) * kRows + r), q >> 1));
+          l[q] = dsmem_ld_f32(dsmem_map(l_l + 4 * ((q & 1) * kRows + r), q >> 1));
+          mmax = fmaxf(mmax, m[q]);
+        }
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2 * kMaxCluster; ++q) {
+        if (q < ns) {
+          m[q] = m[q] == -INFINITY ? 0.f : fast_exp2(m[q] - mmax);
+          lsum += m[q] * l[q];
+        }
+      }
+      const float inv = 1.f / lsum;
+#pragma unroll
+      for (int q = 0; q < 2 * kMaxCluster; ++q)
+        if (q < ns) w_s[(r - r_lo) * 2 * kMaxCluster + q] = m[q] * inv;
+    }
+    __syncthreads();
     for (int e = tid; e < (r_hi - r_lo) * (D / 4); e += kThreads) {
       const int r = r_lo + e / (D / 4);
       const int d4 = e % (D / 4);
       const int i = r / a.Gc, hl = r % a.Gc;
       if (hl >= heads) continue;
-      float mmax = -INFINITY;
-      for (int c = 0; c < a.C; ++c)
-        for (int x = 0; x < 2; ++x) mmax = fmaxf(mmax, dsmem_ld_f32(dsmem_map(m_l + 4 * (x * kRows + r), c)));
-      float lsum = 0.f;
+      const float* w = w_s + (r - r_lo) * 2 * kMaxCluster;
+      const uint32_t off = acc_l + 4 * (r * D + 4 * (d4 ^ (r & 7)));
+      float4 v[2 * kMaxCluster];
+#pragma unroll
+      for (int q = 0; q < 2 * kMaxCluster; ++q)
+        if (q < ns) v[q] = dsmem_ld_f32x4(dsmem_map(off + 4 * (q & 1) * kRows * D, q >> 1));
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < a.C; ++c) {
-        for (int x = 0; x < 2; ++x) {
-          const float mc = dsmem_ld_f32(dsmem_map(m_l + 4 * (x * kRows + r), c));
-          const float w = mc == -INFINITY ? 0.f : fast_exp2(mc - mmax);
-          lsum += w * dsmem_ld_f32(dsmem_map(l_l + 4 * (x * kRows + r), c));
-          const float4 v = dsmem_ld_f32x4(dsmem_map(acc_l + 4 * ((x * kRows + r) * D + 4 * (d4 ^ (r & 7))), c));
-          o.x += w * v.x;
-          o.y += w * v.y;
-          o.z += w * v.z;
-          o.w += w * v.w;
+#pragma unroll
+      for (int q = 0; q < 2 * kMaxCluster; ++q) {
+        if (q < ns) {
+          o.x += w[q] * v[q].x;
+          o.y += w[q] * v[q].y;
+          o.z += w[q] * v[q].z;
+          o.w += w[q] * v[q].w;
         }
       }
-      const float inv = 1.f / lsum;
       uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 4 * d4;
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
     }
   }
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it

@@ -45,7 +45,9 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <memory>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -87,6 +89,17 @@ struct TrainArgs {
   int nq;      // query tiles per stream
   int pairs;   // head slots per KV group: ceil(G / 2)
   int items;   // 2 * nq * batch * Hkv * pairs
+  int planned; // 1: each CTA runs the item list the Plan gives it; 0: items blockIdx.x + n * gridDim.x
+};
+
+// Static schedule: CTA c runs items item[start[c] .. start[c+1]) in that order.  Built
+// on the host by longest-processing-time-first list scheduling (item cost from its
+// key-tile count), which keeps the persistent CTAs' loads within a few percent.
+constexpr int kMaxPlanCtas = 256;
+constexpr int kMaxPlanItems = 8192;
+struct Plan {
+  uint16_t start[kMaxPlanCtas + 1];
+  uint16_t item[kMaxPlanItems];
 };
 
 // SW128 K-major / MN-major shared-memory matrix descriptor (tcgen05 format).
@@ -110,7 +123,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
 // starting at z position noisy_start.
 struct Sched {
   int n_clean, clean_full, n_noisy, noisy_start;
-  __device__ __forceinline__ int count() const { return n_clean + n_noisy; }
+  __host__ __device__ __forceinline__ int count() const { return n_clean + n_noisy; }
   __device__ __forceinline__ void at(int n, int& kstart, bool& noisy, bool& partial) const {
     if (n < n_clean) {
       kstart = kBN * n;
@@ -124,7 +137,7 @@ struct Sched {
   }
 };
 
-__device__ __forceinline__ Sched make_sched(bool noisy_q, int j, int L, int B) {
+__host__ __device__ __forceinline__ Sched make_sched(bool noisy_q, int j, int L, int B) {
   Sched s;
   if (!noisy_q) {
     const int rows_end = min(kBM * j + kBM, L);
@@ -153,7 +166,7 @@ struct Item {
   Sched sched;
 };
 
-__device__ __forceinline__ Item item_of(const TrainArgs& a, int idx) {
+__host__ __device__ __forceinline__ Item item_of(const TrainArgs& a, int idx) {
   Item it;
   const int per_rank = a.batch * a.Hkv * a.pairs;
   const int rank = idx / per_rank;
@@ -172,11 +185,21 @@ __device__ __forceinline__ Item item_of(const TrainArgs& a, int idx) {
   return it;
 }
 
+// The n-th item of this CTA, or -1 past its last.
+__device__ __forceinline__ int nth_item(const Plan& p, const TrainArgs& a, int n) {
+  if (a.planned) {
+    const int j = p.start[blockIdx.x] + n;
+    return j < p.start[blockIdx.x + 1] ? p.item[j] : -1;
+  }
+  const int idx = blockIdx.x + n * gridDim.x;
+  return idx < a.items ? idx : -1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     train_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                      const TrainArgs a) {
+                      const TrainArgs a, const __grid_constant__ Plan plan) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -217,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int kt = 0, t = 0;  // CTA-local key-tile and item counters
-      for (int idx = blockIdx.x; idx < a.items; idx += gridDim.x, ++t) {
+      for (int idx; (idx = nth_item(plan, a, t)) >= 0; ++t) {
         const Item it = item_of(a, idx);
         if (t > 0 && !mbar_wait(&bar_q_empty, (t - 1) & 1)) {
           set_status(a.status, MARS_DEV_TIMEOUT);
@@ -304,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      for (int idx = blockIdx.x; ok && idx < a.items; idx += gridDim.x, ++t) {
+      for (int idx; ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
         const Item it = item_of(a, idx);
         const int nt = it.sched.count();
         wait_all(&bar_q_full, t & 1);
@@ -356,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
     int cs = 0, co = 0;  // S-ready and O-ready phases consumed
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < a.items; idx += gridDim.x) {
+    for (int t = 0, idx; ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
       const Item it = item_of(a, idx);
       if (x == 1 && !it.two_q) continue;
       const int h = it.h_a + x;
@@ -565,9 +588,54 @@ bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// LPT plan for (shape, grid), cached: item cost = key tiles (x 0.6 for a single-head
+// item) + a per-item overhead of about 2.5 tiles, all in tenths of a tile.
+const Plan* plan_for(const TrainArgs& a, int D, int grid) {
+  if (grid > kMaxPlanCtas || a.items > kMaxPlanItems) return nullptr;
+  struct Entry {
+    long long key[8];
+    std::unique_ptr<Plan> plan;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  const long long key[8] = {a.batch, a.L, a.B, a.Hq, a.Hkv, D, grid, 0};
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (std::equal(key, key + 8, e.key)) return e.plan.get();
+  std::vector<int> cost(a.items), order(a.items);
+  for (int i = 0; i < a.items; ++i) {
+    const Item it = item_of(a, i);
+    cost[i] = it.sched.count() * (it.two_q ? 10 : 6) + 25;
+    order[i] = i;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+  std::vector<long long> load(grid, 0);
+  std::vector<std::vector<int>> lists(grid);
+  for (int i : order) {
+    int best = 0;
+    for (int c = 1; c < grid; ++c)
+      if (load[c] < load[best]) best = c;
+    load[best] += cost[i];
+    lists[best].push_back(i);
+  }
+  std::unique_ptr<Plan> p(new Plan());
+  int j = 0;
+  for (int c = 0; c < grid; ++c) {
+    p->start[c] = static_cast<uint16_t>(j);
+    for (int i : lists[c]) p->item[j++] = static_cast<uint16_t>(i);
+  }
+  p->start[grid] = static_cast<uint16_t>(j);
+  if (cache.size() >= 16) cache.erase(cache.begin());
+  Entry e;
+  std::copy(key, key + 8, e.key);
+  e.plan = std::move(p);
+  cache.push_back(std::move(e));
+  return cache.back().plan.get();
+}
+
 template <int D>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-           const TrainArgs& a, cudaStream_t stream) {
+           TrainArgs a, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     const cudaError_t e =
@@ -576,7 +644,10 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
     configured = true;
   }
   const int grid = std::min(a.items, mars_host::num_sms());
-  train_attn_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(tq, tk, tv, to, a);
+  static Plan none;  // unused when a.planned == 0
+  const Plan* plan = plan_for(a, D, grid);
+  a.planned = plan != nullptr ? 1 : 0;
+  train_attn_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(tq, tk, tv, to, a, plan != nullptr ? *plan : none);
   return mars_host::launch_status();
 }
 
@@ -617,6 +688,7 @@ extern "C" int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint1
   a.nq = nq;
   a.pairs = (a.G + 1) / 2;
   a.items = 2 * nq * batch * Hkv * a.pairs;
+  a.planned = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return D == 64 ? launch<64>(tq, tk, tv, to, a, s) : launch<128>(tq, tk, tv, to, a, s);
 }
