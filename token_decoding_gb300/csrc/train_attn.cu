@@ -312,17 +312,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) return;
         ++cp[x];
         tc_fence_after();
-        const uint32_t s_col = tmem + x * kBN;  // P_hi in columns [0, 64), P_lo in [64, 128)
+        const uint32_t s_col = tmem + x * kBN;  // P over the columns of S_x
         const uint32_t o_col = tmem + C::O_COL + x * D;
         const uint64_t vb = desc_v + ((st * C::KV_BYTES) >> 4);
         if (leader) {
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            tc_mma_ts(o_col, s_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
-          if (split) {
+          if (!split) {
 #pragma unroll
             for (int ks = 0; ks < kBN / 16; ++ks)
-              tc_mma_ts(o_col, s_col + 64 + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, 1u);
+              tc_mma_ts(o_col, s_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
+          } else {
+            // keys [16 ks, 16 ks + 16): hi at column 32 (ks / 2) + 8 (ks % 2), lo 16 columns later
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+              const uint32_t pc = s_col + 32 * (ks >> 1) + 8 * (ks & 1);
+              tc_mma_ts(o_col, pc, vb + ((ks * 16 * 128) >> 4), id_pv, (!first || ks > 0) ? 1u : 0u);
+              tc_mma_ts(o_col, pc + 16, vb + ((ks * 16 * 128) >> 4), id_pv, 1u);
+            }
           }
         }
         __syncwarp();
@@ -412,26 +417,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         // visible columns of this row inside the tile: [vlo, vhi] (empty when vlo > vhi)
         const int vlo = part ? max((nz ? n_lo_v : 0) - kstart, 0) : 0;
         const int vhi = part ? min((nz ? n_hi_v : c_hi_v) - kstart, kBN - 1) : kBN - 1;
-        uint32_t s[kBN];
+        // D = 64: one pass, all of S in registers (the softmax is the bottleneck here).
+        // D = 128: two passes over S in TMEM, 64 columns at a time (half the registers):
+        // the row max, then exp2 and the bf16 store of P.  Hidden scores become -inf
+        // (exp2 of them is exactly 0).
+        constexpr int SPAN = D == 64 ? kBN : 64;  // columns held in registers at a time
+        auto load_span = [&](int h, uint32_t (&v)[SPAN]) {
 #pragma unroll
-        for (int c = 0; c < kBN; c += 32) {
-          uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[c]);
-          tmem_ld32(s_col + c, chunk);
-        }
-        tc_wait_ld();
-        // hidden scores become -inf (exp2 of them is exactly 0)
-        if (part) {
+          for (int c = 0; c < SPAN; c += 32) tmem_ld32(s_col + SPAN * h + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
+          tc_wait_ld();
+          if (part) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) s[c] = (c >= vlo && c <= vhi) ? s[c] : 0xFF800000u;
-        }
-        // row max (scale > 0 commutes with max)
+            for (int c = 0; c < SPAN; ++c) v[c] = (SPAN * h + c >= vlo && SPAN * h + c <= vhi) ? v[c] : 0xFF800000u;
+          }
+        };
+        auto span_max = [&](const uint32_t (&v)[SPAN], float& m0, float& m1, float& m2, float& m3) {
+#pragma unroll
+          for (int c = 0; c < SPAN; c += 4) {
+            m0 = fmaxf(m0, __uint_as_float(v[c]));
+            m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
+            m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
+            m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+          }
+        };
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBN; c += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-          mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+        uint32_t v0[SPAN];  // D = 64: S, kept for the exp pass
+        if constexpr (SPAN == kBN) {
+          load_span(0, v0);
+          span_max(v0, mx0, mx1, mx2, mx3);
+        } else {
+#pragma unroll 1
+          for (int h = 0; h < kBN / SPAN; ++h) {
+            load_span(h, v0);
+            span_max(v0, mx0, mx1, mx2, mx3);
+          }
         }
         const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
         // lazy rescale: keep the old reference max unless the new one is 2^8 larger.
@@ -443,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = tile_max;
         }
         if (n > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < D; c += 16) {
             uint32_t ov[16];
             tmem_ld16(o_col + c, ov);
@@ -454,44 +473,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float neg_mu = m_used == -INFINITY ? 0.f : -m_used;
-        // P = exp2(s * scale_log2 - mu) as bf16 pairs over S in TMEM (all of S is in
-        // registers): hi in columns [0, 64); on partial tiles lo = P - hi in [64, 128)
+        // P = exp2(s * scale_log2 - mu) as bf16 pairs, written over S columns already read:
+        // keys [32q, 32q + 32) -> hi in columns [16q, 16q + 16); on split tiles hi in
+        // [32q, 32q + 16) and lo = P - hi in [32q + 16, 32q + 32).
         float sum0 = 0.f, sum1 = 0.f;
-        if (!split) {
+#pragma unroll 1
+        for (int h = 0; h < kBN / SPAN; ++h) {
+          if constexpr (SPAN != kBN) load_span(h, v0);
 #pragma unroll
-          for (int c = 0; c < kBN; c += 32) {
-            uint32_t hi[16];
+          for (int qq = 0; qq < SPAN / 32; ++qq) {
+            const int q = (SPAN / 32) * h + qq;
+            if (!split) {
+              uint32_t hi[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e]), a.scale_log2, neg_mu));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e + 1]), a.scale_log2, neg_mu));
-              sum0 += p0;
-              sum1 += p1;
-              hi[e] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(s_col + (c >> 1), hi);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kBN; c += 16) {
-            uint32_t hi[8], lo[8];
-            if (!__any_sync(0xffffffffu, vlo <= c + 15 && vhi >= c && vlo <= vhi)) {
-              // no row of this warp sees these 16 keys
-#pragma unroll
-              for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0u;
+              for (int e = 0; e < 16; ++e) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e]), a.scale_log2, neg_mu));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2, neg_mu));
+                sum0 += p0;
+                sum1 += p1;
+                hi[e] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16(s_col + 16 * q, hi);
             } else {
+              uint32_t hi[16], lo[16];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e]), a.scale_log2, neg_mu));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(s[c + 2 * e + 1]), a.scale_log2, neg_mu));
+              for (int e = 0; e < 16; ++e) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e]), a.scale_log2, neg_mu));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2, neg_mu));
                 sum0 += p0;
                 sum1 += p1;
                 hi[e] = pack_bf16x2(p0, p1);
                 lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
               }
+              tmem_st16(s_col + 32 * q, hi);
+              tmem_st16(s_col + 32 * q + 16, lo);
             }
-            tmem_st8(s_col + (c >> 1), hi);
-            tmem_st8(s_col + 64 + (c >> 1), lo);
           }
         }
         l = l * alpha + (sum0 + sum1);
