@@ -48,6 +48,27 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// max(a, b, c) in one instruction (the three-input form of sm_100-class GPUs).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (r0, r1) = (x0, x1) * s + t with one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2(float x0, float x1, float s, float t, float& r0, float& r1) {
+  asm("{\n .reg .b64 x, c, b, r;\n mov.b64 x, {%2, %3};\n mov.b64 c, {%4, %4};\n mov.b64 b, {%5, %5};\n"
+      " fma.rn.f32x2 r, x, c, b;\n mov.b64 {%0, %1}, r;\n}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(t));
+}
+// acc (two fp32 lanes) += (e0, e1) with one packed fp32x2 add.
+__device__ __forceinline__ void add2(uint64_t& acc, float e0, float e1) {
+  asm("{\n .reg .b64 e;\n mov.b64 e, {%1, %2};\n add.rn.f32x2 %0, %0, e;\n}\n" : "+l"(acc) : "f"(e0), "f"(e1));
+}
+__device__ __forceinline__ float sum2(uint64_t acc) {
+  return __uint_as_float(static_cast<uint32_t>(acc)) + __uint_as_float(static_cast<uint32_t>(acc >> 32));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

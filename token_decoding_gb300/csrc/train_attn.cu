@@ -433,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto span_max = [&](const uint32_t (&v)[SPAN], float& m0, float& m1, float& m2, float& m3) {
 #pragma unroll
-          for (int c = 0; c < SPAN; c += 4) {
-            m0 = fmaxf(m0, __uint_as_float(v[c]));
-            m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
-            m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
-            m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+          for (int c = 0; c < SPAN; c += 8) {
+            m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+            m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
           }
         };
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = exp2(s * scale_log2 - mu) as bf16 pairs, written over S columns already read:
         // keys [32q, 32q + 32) -> hi in columns [16q, 16q + 16); on split tiles hi in
         // [32q, 32q + 16) and lo = P - hi in [32q + 16, 32q + 32).
-        float sum0 = 0.f, sum1 = 0.f;
+        uint64_t sum2x = 0;  // two fp32 partial sums (bits of +0.0f)
 #pragma unroll 1
         for (int h = 0; h < kBN / SPAN; ++h) {
           if constexpr (SPAN != kBN) load_span(h, v0);
@@ -487,10 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t hi[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e]), a.scale_log2, neg_mu));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2, neg_mu));
-                sum0 += p0;
-                sum1 += p1;
+                float x0, x1;
+                fma2(__uint_as_float(v0[32 * qq + 2 * e]), __uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2,
+                     neg_mu, x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                add2(sum2x, p0, p1);
                 hi[e] = pack_bf16x2(p0, p1);
               }
               tmem_st16(s_col + 16 * q, hi);
@@ -498,10 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t hi[16], lo[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e]), a.scale_log2, neg_mu));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2, neg_mu));
-                sum0 += p0;
-                sum1 += p1;
+                float x0, x1;
+                fma2(__uint_as_float(v0[32 * qq + 2 * e]), __uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2,
+                     neg_mu, x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                add2(sum2x, p0, p1);
                 hi[e] = pack_bf16x2(p0, p1);
                 lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
               }
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        l = l * alpha + (sum0 + sum1);
+        l = l * alpha + sum2(sum2x);
         tc_wait_st();
         tc_fence_before();
         mbar_arrive(&bar_p[x]);
