@@ -589,6 +589,39 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """--profile PART: warm-up + steps launches of one kernel on its workload, nothing else (for ncu)."""
+    import torch
+
+    import token_decoding_gb300 as mars
+    from token_decoding_gb300 import build as mars_build
+    from token_decoding_gb300 import synth
+
+    if not os.path.exists(mars._lib.LIB_PATH):
+        mars_build.build()
+    device = torch.device("cuda:0")
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234)
+    part = args.profile
+    if part.startswith("train"):
+        w = TrainWork(synth.TRAIN_05B if part == "train_05b" else synth.TRAIN_7B, device, gen, 0)
+        run = lambda i: w.run(mars, i)  # noqa: E731
+    else:
+        shape = synth.DECODE_7B_B64 if part.endswith("b64") else synth.DECODE_7B_B1
+        w = DecodeWork(shape, device, gen, 0, steps_per_episode=shape.steps)
+        n_out = torch.zeros((shape.batch,), dtype=torch.int32, device=device)
+        if part.startswith("decode"):
+            run = lambda i: w.run_decode(mars, i)  # noqa: E731
+        else:
+            def run(i):
+                w.reset()
+                w.run_accept(mars, i, n_out)
+    for i in range(args.warmup + args.steps):
+        run(i)
+    torch.cuda.synchronize()
+    print("profiled", part, args.warmup + args.steps, "launches")
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -598,9 +631,15 @@ def main():
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph batch-1 decode loop")
+    p.add_argument("--profile", choices=["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1",
+                                         "accept_b1"],
+                   help="only launch this kernel, warm-up + steps times, and print no JSON (for ncu)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
+    if args.profile:
+        run_profile(args)
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
