@@ -619,11 +619,11 @@ extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const 
   a.nhc = ceil_div(a.G, a.Gc);
   const long long units = static_cast<long long>(batch) * Hkv * a.nhc;
   MARS_HOST_CHECK(units * kMaxCluster < (1LL << 31), MARS_ERR_INVALID_ARG);
-  // CTAs per unit: about two per SM over the whole grid, at most one per cache
-  // tile of the longest sequence.
+  // CTAs per unit: about one per SM over the whole grid (a CTA's fixed cost is
+  // several tiles' worth), at most one per cache tile of the longest sequence.
   const int sms = mars_host::num_sms();
   const int max_tiles = std::max(1, ceil_div(max_len, kTileKeys));
-  int cl = pow2_ceil(std::max(1, ceil_div(2LL * sms, units)));
+  int cl = pow2_ceil(std::max(1, ceil_div(sms, units)));
   cl = std::min(cl, kMaxCluster);
   while (cl > 1 && cl > max_tiles) cl >>= 1;
   a.C = cl;
