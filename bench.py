@@ -262,10 +262,10 @@ class DecodeWork:
         st = self.sets[step % self.nsets]
         mars.decode_attn(self.q, self.kn, self.vn, st["kc"], st["vc"], st["lens"], self.max_len, o=self.o)
 
-    def run_accept(self, mars, step, n_out):
+    def run_accept(self, mars, step, n_out, gate="prob"):
         st = self.sets[step % self.nsets]
         mars.accept(st["logits"], DECODE_TAU, self.kn, self.vn, st["kc"], st["vc"], st["lens"], workspace=st["ws"],
-                    tokens=self.tokens, conf=self.conf, n_commit=n_out)
+                    tokens=self.tokens, conf=self.conf, n_commit=n_out, gate=gate)
 
     def byte_counts(self, records):
         """Algorithmic bytes of decode and accept per executed step, from the commit history."""
@@ -422,6 +422,8 @@ def run_gpu(args, rank, world, local):
     graph = None if args.no_graph else run_b1_graph(args, mars, dec1, device)
     if graph is not None:
         parts["decode_step_b1"]["graph_steps_per_s"] = graph
+    # the margin gate (a variant of the accept row, timed on its own after the step loop)
+    parts["accept_margin_b64"] = run_margin(args, mars, dec64, device, peaks["hbm_gbs"], traffic)
 
     line = {
         "metric": METRIC,
@@ -442,7 +444,7 @@ def run_gpu(args, rank, world, local):
         "parts": parts,
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": 8 * args.steps,  # 2 train, 2 decode, 2 x (accept stream + finish)
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -483,6 +485,40 @@ def run_e2e(args, mars, work, device, stream, dist, world):
     d2h = ho.numel() * ho.element_size()
     val = work.flops * steps * world / (ms * 1e-3) / 1e12
     return {"value": round(val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_margin(args, mars, work, device, hbm_peak, traffic):
+    """mars_accept_margin on the batch-64 decode workload: min(steps, 64) calls after a
+    cache reset (so the appends stay inside the cache), CUDA events on the stream."""
+    import torch
+
+    s = work.s
+    n = max(1, min(args.steps, 64))
+    stream = torch.cuda.current_stream()
+    n_out = torch.zeros((n + args.warmup, s.batch), dtype=torch.int32, device=device)
+
+    def call(i):
+        st = work.sets[i % work.nsets]
+        mars.accept(st["logits"], DECODE_TAU, work.kn, work.vn, st["kc"], st["vc"], st["lens"], workspace=st["ws"],
+                    tokens=work.tokens, conf=work.conf, n_commit=n_out[i], gate="margin")
+
+    work.reset()
+    for i in range(args.warmup):
+        call(i)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(args.warmup, args.warmup + n):
+        call(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1])
+    committed = int(n_out[args.warmup:].sum().item())
+    bytes_ = n * (s.batch * s.B * s.V * 2 + s.batch * s.B * 8 + s.batch * 8) + committed * s.Hkv * s.D * 2 * 2 * 2
+    achieved = bytes_ / (ms * 1e-3) / 1e9
+    work.reset()
+    return {"avg_us": round(ms / n * 1e3, 3), "calls": n,
+            "roofline": roofline("hbm", achieved, hbm_peak, "GB/s", traffic.get("accept_margin_b64"))}
 
 
 def run_b1_graph(args, mars, work, device):
@@ -613,9 +649,11 @@ def run_profile(args):
         if part.startswith("decode"):
             run = lambda i: w.run_decode(mars, i)  # noqa: E731
         else:
+            gate = "margin" if "margin" in part else "prob"
+
             def run(i):
                 w.reset()
-                w.run_accept(mars, i, n_out)
+                w.run_accept(mars, i, n_out, gate)
     for i in range(args.warmup + args.steps):
         run(i)
     torch.cuda.synchronize()
@@ -632,7 +670,7 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph batch-1 decode loop")
     p.add_argument("--profile", choices=["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1",
-                                         "accept_b1"],
+                                         "accept_b1", "accept_margin_b64"],
                    help="only launch this kernel, warm-up + steps times, and print no JSON (for ncu)")
     args = p.parse_args()
     if args.warmup < 3:

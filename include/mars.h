@@ -146,6 +146,26 @@ int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau,
                 int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mars_accept_margin - mars_accept with the margin gate.  The authors' MARS blog
+ * post ("Inference: a knob, not a mode switch") reports that gating on how far
+ * ahead the top token is, rather than on its probability, holds up better on
+ * format-heavy text.  The margin is read as p1 - p2: the top-1 probability
+ * minus the largest probability of any other token, at temperature 1.
+ *
+ * Same arguments, workspace, outputs and error behaviour as mars_accept,
+ * except that conf[b, i] holds the margin p1 - p2 (0 when two tokens tie at the
+ * maximum, p1 when V == 1) and a position passes while conf >= tau.  It is
+ * computed in the same single pass over the logits (the second largest logit
+ * is tracked beside the maximum): p1 - p2 = (1 - exp(l2 - m)) / sum exp(l - m).
+ */
+int mars_accept_margin(const uint16_t* logits, int batch, int B, int V, float tau,
+                       const uint16_t* k_new, const uint16_t* v_new,
+                       uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
+                       int Hkv, int D, int cap,
+                       int32_t* tokens, float* conf, int32_t* n_commit,
+                       int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mars_accept_noalloc - mars_accept for callers that cannot allocate device
  * memory.  The MARS pages have no counterpart to this call: it exists for
  * callers such as plugins that only receive the input and output buffers of a

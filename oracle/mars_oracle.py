@@ -21,13 +21,16 @@ Sources (cited by page title and section / equation):
 Everything is float64.  bf16 inputs arrive as float64 arrays holding the
 exactly widened bf16 values.
 
-Readings taken where the pages are silent (each one is listed in the design doc):
+Readings taken where the pages are silent:
 
 * softmax scale is a parameter (the kernels are called with 1/sqrt(D));
 * GQA: query head h uses KV head h // (Hq // Hkv) (contiguous groups);
 * L need not be a multiple of B: ceil() makes the last block short;
 * confidence = top-1 softmax probability at temperature 1; a position passes
   when conf >= tau; ties in the argmax go to the lowest vocabulary index;
+* the margin gate ([blog] "Inference": how far ahead the top token is) is read
+  as p1 - p2, the top-1 probability minus the largest probability of any
+  other token;
 * the block-level KV cache advances per sequence by that sequence's own
   commit count (the batch-minimum variant is not part of this oracle).
 
@@ -174,13 +177,17 @@ def decode_attn(q, k_new, v_new, k_cache, v_cache, cache_len, scale: float):
 # [news] "at least one token")
 # --------------------------------------------------------------------------
 
-def accept_rows(logits):
-    """Per proposal position: greedy token and its top-1 probability.
+def accept_rows(logits, gate: str = "prob"):
+    """Per proposal position: greedy token and its confidence.
 
-    logits: [..., V] float64 (finite).  Returns (tokens int64, conf float64):
-    m = max_v l_v; token = the smallest v with l_v = m; conf = 1 / sum_v
-    exp(l_v - m), which is softmax(l)[token] at temperature 1.
+    logits: [..., V] float64 (finite).  m = max_v l_v; token = the smallest v
+    with l_v = m.  With gate "prob" the confidence is the top-1 probability
+    1 / sum_v exp(l_v - m) = softmax(l)[token] at temperature 1 ([blog]
+    "Inference").  With gate "margin" it is how far ahead the top token is,
+    read as p1 - p2: softmax(l)[token] minus the largest softmax(l)[v] over the
+    other v (0 when two tokens tie at the max; p1 when V == 1).
     """
+    assert gate in ("prob", "margin")
     x = np.asarray(logits, dtype=np.float64)
     assert np.all(np.isfinite(x)), "logits must be finite"
     flat = x.reshape(-1, x.shape[-1])
@@ -189,8 +196,15 @@ def accept_rows(logits):
     for r in range(flat.shape[0]):
         row = flat[r]
         m = row.max()
-        tokens[r] = np.flatnonzero(row == m)[0]
-        conf[r] = 1.0 / np.exp(row - m).sum()
+        tok = int(np.flatnonzero(row == m)[0])
+        tokens[r] = tok
+        if gate == "prob":
+            conf[r] = 1.0 / np.exp(row - m).sum()
+        else:
+            p = np.exp(row - m)
+            p /= p.sum()
+            others = np.delete(p, tok)
+            conf[r] = p[tok] - (others.max() if others.size else 0.0)
     return tokens.reshape(x.shape[:-1]), conf.reshape(x.shape[:-1])
 
 
@@ -209,9 +223,9 @@ def commit_count(conf_row, tau: float) -> int:
     return max(n, 1)
 
 
-def accept(logits, tau: float):
-    """tokens [b, B], conf [b, B], n_commit [b] for logits [b, B, V]."""
-    tokens, conf = accept_rows(logits)
+def accept(logits, tau: float, gate: str = "prob"):
+    """tokens [b, B], conf [b, B], n_commit [b] for logits [b, B, V] (gate: see accept_rows)."""
+    tokens, conf = accept_rows(logits, gate)
     n = np.array([commit_count(conf[b], tau) for b in range(conf.shape[0])], dtype=np.int64)
     return tokens, conf, n
 

@@ -25,20 +25,25 @@ def max_abs(a, b):
 ATTN_TOL = 1e-2  # max |delta| for bf16 outputs with fp32 accumulation
 
 
-def check_accept(tokens, conf, n_commit, logits64, tau):
+def check_accept(tokens, conf, n_commit, logits64, tau, gate="prob"):
     """Compare a GPU accept result with the fp64 oracle.
 
-    Tokens must match exactly and conf to 1e-5 relative.  A commit count may
+    Tokens must match exactly; conf to 1e-5 relative (top-1 probability) or
+    2e-6 absolute (margin p1 - p2, which is 0 on ties).  A commit count may
     differ only where the first position whose pass/fail decision differs has
     an fp64 confidence within 1e-4 of tau; such positions are returned as a
     report (b, position) instead of failing.
     """
     import oracle
 
-    t_o, c_o, n_o = oracle.accept(logits64, tau)
+    t_o, c_o, n_o = oracle.accept(logits64, tau, gate)
     assert np.array_equal(tokens, t_o), np.argwhere(tokens != t_o)[:8]
-    rel = np.abs(conf.astype(np.float64) - c_o) / c_o
-    assert float(rel.max()) < 1e-5, float(rel.max())
+    if gate == "prob":
+        rel = np.abs(conf.astype(np.float64) - c_o) / c_o
+        assert float(rel.max()) < 1e-5, float(rel.max())
+    else:
+        err = np.abs(conf.astype(np.float64) - c_o)
+        assert float(err.max()) < 2e-6, float(err.max())
     near = oracle.near_threshold(c_o, tau)
     report = []
     for b in range(n_o.shape[0]):

@@ -353,6 +353,46 @@ def check_accept_vs_library(accept_rows):
             assert abs(conf[b, i] - softmax(x[b, i]).max()) < 1e-12
 
 
+def check_margin_closed_forms(accept_rows):
+    """Margin gate p1 - p2: closed forms on rows whose softmax is known by hand."""
+    # V = 2: p1 - p2 = tanh(|l1 - l2| / 2)
+    for a, b in [(1.0, 0.0), (0.0, 3.5), (-2.0, -2.25), (7.0, 7.0)]:
+        tok, conf = accept_rows(np.array([[[a, b]]]), "margin")
+        assert tok[0, 0] == (0 if a >= b else 1)
+        assert abs(conf[0, 0] - np.tanh(abs(a - b) / 2)) < 1e-15
+    # one spike of height x over V - 1 zeros: (e^x - 1) / (e^x + V - 1)
+    V = 1000
+    for x, j in [(8.0, 17), (3.0, 999), (0.5, 0)]:
+        row = np.zeros(V)
+        row[j] = x
+        tok, conf = accept_rows(row[None, None, :], "margin")
+        assert tok[0, 0] == j
+        assert abs(conf[0, 0] - np.expm1(x) / (np.exp(x) + V - 1)) < 1e-13
+    # two tokens tie at the max: zero margin; a single token: margin 1
+    row = np.zeros((1, 1, 64))
+    row[0, 0, [5, 40]] = 3.0
+    _, conf = accept_rows(row, "margin")
+    assert conf[0, 0] == 0.0
+    _, conf = accept_rows(np.array([[[1.5]]]), "margin")
+    assert conf[0, 0] == 1.0
+
+
+def check_margin_vs_library(accept_rows):
+    """Margin gate against scipy's softmax sorted by numpy, and its bounds."""
+    from scipy.special import softmax
+
+    x = rand((3, 5, 501), 45, sigma=2.0)
+    x = np.round(x * 4) / 4  # coarse grid: ties at the max happen
+    tok_p, p1 = accept_rows(x, "prob")
+    tok, conf = accept_rows(x, "margin")
+    assert np.array_equal(tok, tok_p)
+    for b in range(3):
+        for i in range(5):
+            top = np.sort(softmax(x[b, i]))[::-1]
+            assert abs(conf[b, i] - (top[0] - top[1])) < 1e-12
+    assert np.all(conf <= p1 + 1e-15) and np.all(conf >= 2 * p1 - 1 - 1e-15) and np.all(conf >= 0)
+
+
 def check_commit_rule(commit_count):
     assert commit_count([0.5, 0.99, 0.99, 0.99], 0.9) == 1      # first below tau: still one token
     assert commit_count([0.99, 0.99, 0.5, 0.99], 0.9) == 2      # stop at the first below tau

@@ -42,6 +42,8 @@ def all_pins(m):
         "accept_closed": lambda: pins.check_accept_one_hot_closed_form(m.accept_rows),
         "accept_ties": lambda: pins.check_accept_ties_lowest_index(m.accept_rows),
         "accept_lib": lambda: pins.check_accept_vs_library(m.accept_rows),
+        "margin_closed": lambda: pins.check_margin_closed_forms(m.accept_rows),
+        "margin_lib": lambda: pins.check_margin_vs_library(m.accept_rows),
         "commit": lambda: pins.check_commit_rule(m.commit_count),
         "tau": lambda: pins.check_accept_tau_extremes(m.accept),
         "append": lambda: pins.check_append(m.append_kv),
@@ -79,9 +81,18 @@ MUTATIONS = [
     # decode reads the wrong KV head
     ("            g = h // group\n            keys =", "            g = 0\n            keys ="),
     # argmax ties go to the last index
-    ("tokens[r] = np.flatnonzero(row == m)[0]", "tokens[r] = np.flatnonzero(row == m)[-1]"),
+    ("tok = int(np.flatnonzero(row == m)[0])", "tok = int(np.flatnonzero(row == m)[-1])"),
     # confidence taken as the sum instead of its inverse
     ("conf[r] = 1.0 / np.exp(row - m).sum()", "conf[r] = np.exp(row - m).sum() / row.size"),
+    # margin: the top token is not removed before taking the runner-up (always 0)
+    ("others = np.delete(p, tok)", "others = p"),
+    # margin: the smallest other probability instead of the largest
+    ("conf[r] = p[tok] - (others.max() if others.size else 0.0)",
+     "conf[r] = p[tok] - (others.min() if others.size else 0.0)"),
+    # margin: runner-up of a one-token vocabulary taken as p1 (margin 0 instead of 1)
+    ("(others.max() if others.size else 0.0)", "(others.max() if others.size else p[tok])"),
+    # margin: unnormalised (logit-domain) difference
+    ("            p /= p.sum()\n", ""),
     # strict > instead of >= tau
     ("if c >= tau:", "if c > tau:"),
     # the at-least-one rule dropped

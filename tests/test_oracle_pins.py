@@ -101,6 +101,14 @@ def test_accept_matches_scipy_and_numpy():
     pins.check_accept_vs_library(oracle.accept_rows)
 
 
+def test_margin_closed_forms():
+    pins.check_margin_closed_forms(oracle.accept_rows)
+
+
+def test_margin_matches_scipy_and_bounds():
+    pins.check_margin_vs_library(oracle.accept_rows)
+
+
 def test_commit_rule():
     pins.check_commit_rule(oracle.commit_count)
 

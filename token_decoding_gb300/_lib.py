@@ -40,6 +40,7 @@ _SIGNATURES = {
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
     "mars_accept": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "mars_accept_margin": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_noalloc": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
 }
 
@@ -188,10 +189,13 @@ def accept_workspace(batch: int, B: int, V: int, device) -> torch.Tensor:
 
 
 def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, workspace=None, tokens=None, conf=None,
-           n_commit=None, status=None, stream=None):
-    """Greedy tokens, top-1 probabilities, left-to-right commit and KV append
-    (include/mars.h: mars_accept).  Returns (tokens, conf, n_commit); k_cache,
-    v_cache and cache_len are updated in place."""
+           n_commit=None, status=None, stream=None, gate: str = "prob"):
+    """Greedy tokens, confidences, left-to-right commit and KV append
+    (include/mars.h: mars_accept, or mars_accept_margin with gate="margin", where
+    conf is p1 - p2).  Returns (tokens, conf, n_commit); k_cache, v_cache and
+    cache_len are updated in place."""
+    if gate not in ("prob", "margin"):
+        raise ValueError(f"gate must be 'prob' or 'margin', got {gate!r}")
     nb, bq, V = logits.shape
     hkv, d = k_new.shape[2], k_new.shape[3]
     cap = k_cache.shape[2]
@@ -215,9 +219,9 @@ def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, worksp
     _check(n_commit, "n_commit", torch.int32, (nb,), dev)
     if status is not None:
         _check(status, "status", torch.int32, (1,), dev)
-    _call("mars_accept", _ptr(logits), nb, bq, V, float(tau), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
-          _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
-          _ptr(workspace), workspace.numel(), _stream(stream))
+    _call("mars_accept_margin" if gate == "margin" else "mars_accept", _ptr(logits), nb, bq, V, float(tau),
+          _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens),
+          _ptr(conf), _ptr(n_commit), _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream))
     return tokens, conf, n_commit
 
 

@@ -48,24 +48,27 @@ struct RowState {
   float m;   // running max (-inf when empty)
   int idx;   // smallest index holding m
   float s;   // sum of exp(x - m)
+  float m2;  // second largest value, counting a repeat of m (-inf when none); margin gate only
 };
 
 struct __align__(16) Partial {
   float m;
   int idx;
   float s;
-  int pad;
+  float m2;
 };
 
-__device__ __forceinline__ RowState empty_state() { return RowState{-INFINITY, 0x7fffffff, 0.f}; }
+__device__ __forceinline__ RowState empty_state() { return RowState{-INFINITY, 0x7fffffff, 0.f, -INFINITY}; }
 
-// Merge b into a: the larger max wins, equal maxima keep the lower index.
+// Merge b into a: the larger max wins, equal maxima keep the lower index; the
+// runner-up is the larger of the smaller max and the two runners-up.
 __device__ __forceinline__ void merge(RowState& a, const RowState& b) {
   if (b.m == -INFINITY) return;
   if (a.m == -INFINITY) {
     a = b;
     return;
   }
+  a.m2 = fmaxf(fminf(a.m, b.m), fmaxf(a.m2, b.m2));
   if (b.m > a.m) {
     a.s = a.s * fast_exp2((a.m - b.m) * kLog2e) + b.s;
     a.m = b.m;
@@ -83,6 +86,7 @@ __device__ __forceinline__ RowState shfl_state(const RowState& a, int lane_mask)
   b.m = __shfl_xor_sync(0xffffffffu, a.m, lane_mask);
   b.idx = __shfl_xor_sync(0xffffffffu, a.idx, lane_mask);
   b.s = __shfl_xor_sync(0xffffffffu, a.s, lane_mask);
+  b.m2 = __shfl_xor_sync(0xffffffffu, a.m2, lane_mask);
   return b;
 }
 
@@ -93,11 +97,22 @@ __device__ __forceinline__ RowState warp_reduce(RowState st) {
 }
 
 // Add one scalar element (index order not assumed).
-__device__ __forceinline__ void add_scalar(RowState& st, float x, int idx) { merge(st, RowState{x, idx, 1.f}); }
+__device__ __forceinline__ void add_scalar(RowState& st, float x, int idx) {
+  merge(st, RowState{x, idx, 1.f, -INFINITY});
+}
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// Top two of the values seen so far in each half of a packed bf16 pair (t1 >= t2).
+__device__ __forceinline__ void top2_pair(uint32_t& t1, uint32_t& t2, uint32_t w) {
+  t2 = bmax2(t2, bmin2(t1, w));
+  t1 = bmax2(t1, w);
 }
 
 // acc2 (+)= exp2(x * log2e + mneg) for the two bf16 values packed in w, using
@@ -135,6 +150,7 @@ struct AcceptArgs {
   float* conf;
   int32_t* n_commit;
   int32_t* status;
+  int margin;           // 1: conf = p1 - p2 (margin gate); 0: conf = p1
   Partial* partials;    // [rows][chunks]
   int chunks;           // chunks per row
   int items;            // rows * chunks
@@ -169,7 +185,7 @@ constexpr int kPrefetch = 4;
 
 __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs a) {
   __shared__ float s_conf[16];
-  __shared__ int s_n, s_len;
+  __shared__ int s_n;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vec_per_row = a.D >> 3;
@@ -192,11 +208,12 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
     RowState mg = empty_state();
     for (int s = lane; s < a.chunks; s += 32) {
       const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partials + static_cast<size_t>(r) * a.chunks + s));
-      merge(mg, RowState{p.x, __float_as_int(p.y), p.z});
+      merge(mg, RowState{p.x, __float_as_int(p.y), p.z, p.w});
     }
     const RowState st = warp_reduce(mg);
     if (lane == 0) {
-      const float conf = 1.0f / st.s;
+      // p1 = 1 / s; margin gate: p1 - p2 = (1 - exp(m2 - m)) / s (0 on a tie, p1 if no runner-up)
+      const float conf = a.margin ? (1.0f - fast_exp2((st.m2 - st.m) * kLog2e)) / st.s : 1.0f / st.s;
       a.tokens[r] = st.idx;
       a.conf[r] = conf;
       s_conf[warp] = conf;
@@ -240,6 +257,7 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
   }
 }
 
+template <bool kMargin>
 __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a) {
   extern __shared__ __align__(128) uint4 ring[];  // [kSlots][kChunkVec]
   __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots];
@@ -294,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
     uint64_t acc2 = 0;
     int best_step = -1;
     uint4 best[kGroup];
+    uint32_t t1 = 0xff80ff80u, t2 = 0xff80ff80u;  // margin gate: per-half top two (bf16 -inf)
 #pragma unroll 2
     for (int step = 0; step < kSteps; ++step) {
       uint4 w[kGroup];
@@ -301,6 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
       for (int u = 0; u < kGroup; ++u) {
         const int vi = lane + 32 * (kGroup * step + u);
         w[u] = vi < n ? buf[vi] : kNegInf;
+      }
+      if (kMargin) {
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+          top2_pair(t1, t2, w[u].x);
+          top2_pair(t1, t2, w[u].y);
+          top2_pair(t1, t2, w[u].z);
+          top2_pair(t1, t2, w[u].w);
+        }
       }
       uint32_t mx = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
 #pragma unroll
@@ -337,13 +365,17 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
           if (x == m) found = c.head + 8 * (c.v0 + lane + 32 * (kGroup * best_step + u)) + e;
         }
       }
-      st = RowState{m, found, pair_sum(acc2)};
+      // runner-up of the lane: the smaller half-maximum or either half's second
+      const float m2 = kMargin ? fmaxf(fminf(bf16lo_to_f32(t1), bf16hi_to_f32(t1)),
+                                       fmaxf(bf16lo_to_f32(t2), bf16hi_to_f32(t2)))
+                               : -INFINITY;
+      st = RowState{m, found, pair_sum(acc2), m2};
     }
     // ---- unaligned head (first chunk) and tail (last chunk): at most 7 + 7 elements
     if (k == 0 && lane < c.head) add_scalar(st, bf16lo_to_f32(c.row[lane]), lane);
     if (k == a.chunks - 1 && c.tail0 + lane < a.V) add_scalar(st, bf16lo_to_f32(c.row[c.tail0 + lane]), c.tail0 + lane);
     st = warp_reduce(st);
-    if (lane == 0) a.partials[static_cast<size_t>(r) * a.chunks + k] = Partial{st.m, st.idx, st.s, 0};
+    if (lane == 0) a.partials[static_cast<size_t>(r) * a.chunks + k] = Partial{st.m, st.idx, st.s, st.m2};
   }
 
 }
@@ -367,7 +399,9 @@ int configure_kernel() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MARS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   if (!done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    cudaError_t e = cudaFuncSetAttribute(accept_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(accept_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
     done[dev] = 1;
   }
@@ -380,7 +414,10 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
   a.chunks = chunks_for(a.V);
   a.items = a.batch * a.B * a.chunks;
   const int grid = std::min(a.items, mars_host::num_sms());
-  accept_kernel<<<grid, kThreads, kRingBytes, stream>>>(a);
+  if (a.margin)
+    accept_kernel<true><<<grid, kThreads, kRingBytes, stream>>>(a);
+  else
+    accept_kernel<false><<<grid, kThreads, kRingBytes, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return mars_host::launch_status();
   // The finish launch overlaps its start-up and prefetch with the streaming launch
   // (programmatic dependent launch); it waits for the partials in-kernel.
@@ -440,6 +477,7 @@ AcceptArgs make_args(const uint16_t* logits, int batch, int B, int V, float tau,
   a.conf = conf;
   a.n_commit = n_commit;
   a.status = status;
+  a.margin = 0;
   a.partials = nullptr;
   a.chunks = a.items = 0;
   return a;
@@ -466,6 +504,25 @@ extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, floa
 
   AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
                            conf, n_commit, status);
+  a.partials = static_cast<Partial*>(workspace);
+  return launch(a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mars_accept_margin(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
+                                  const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
+                                  int Hkv, int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit,
+                                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                      conf, n_commit, status);
+  if (rc != MARS_OK) return rc;
+  MARS_HOST_CHECK(workspace != nullptr && mars_host::aligned16(workspace), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(workspace_bytes >= ws_bytes(batch, B, V), MARS_ERR_WORKSPACE_TOO_SMALL);
+  rc = mars_host::check_device();
+  if (rc != MARS_OK) return rc;
+
+  AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                           conf, n_commit, status);
+  a.margin = 1;
   a.partials = static_cast<Partial*>(workspace);
   return launch(a, static_cast<cudaStream_t>(stream));
 }
