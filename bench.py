@@ -422,8 +422,12 @@ def run_gpu(args, rank, world, local):
     graph = None if args.no_graph else run_b1_graph(args, mars, dec1, device)
     if graph is not None:
         parts["decode_step_b1"]["graph_steps_per_s"] = graph
-    # the margin gate (a variant of the accept row, timed on its own after the step loop)
-    parts["accept_margin_b64"] = run_margin(args, mars, dec64, device, peaks["hbm_gbs"], traffic)
+    # variants of the accept row, timed on their own after the step loop: the margin
+    # gate and the batch-minimum cache mode (the paper's original sampler)
+    parts["accept_margin_b64"] = run_accept_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic,
+                                                    "accept_margin_b64", gate="margin")
+    parts["accept_batchmin_b64"] = run_accept_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic,
+                                                      "accept_batchmin_b64", batch_min=True)
 
     line = {
         "metric": METRIC,
@@ -487,8 +491,8 @@ def run_e2e(args, mars, work, device, stream, dist, world):
     return {"value": round(val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
-def run_margin(args, mars, work, device, hbm_peak, traffic):
-    """mars_accept_margin on the batch-64 decode workload: min(steps, 64) calls after a
+def run_accept_variant(args, mars, work, device, hbm_peak, traffic, name, gate="prob", batch_min=False):
+    """An accept variant on the batch-64 decode workload: min(steps, 64) calls after a
     cache reset (so the appends stay inside the cache), CUDA events on the stream."""
     import torch
 
@@ -500,7 +504,7 @@ def run_margin(args, mars, work, device, hbm_peak, traffic):
     def call(i):
         st = work.sets[i % work.nsets]
         mars.accept(st["logits"], DECODE_TAU, work.kn, work.vn, st["kc"], st["vc"], st["lens"], workspace=st["ws"],
-                    tokens=work.tokens, conf=work.conf, n_commit=n_out[i], gate="margin")
+                    tokens=work.tokens, conf=work.conf, n_commit=n_out[i], gate=gate, batch_min=batch_min)
 
     work.reset()
     for i in range(args.warmup):
@@ -518,7 +522,7 @@ def run_margin(args, mars, work, device, hbm_peak, traffic):
     achieved = bytes_ / (ms * 1e-3) / 1e9
     work.reset()
     return {"avg_us": round(ms / n * 1e3, 3), "calls": n,
-            "roofline": roofline("hbm", achieved, hbm_peak, "GB/s", traffic.get("accept_margin_b64"))}
+            "roofline": roofline("hbm", achieved, hbm_peak, "GB/s", traffic.get(name))}
 
 
 def run_b1_graph(args, mars, work, device):

@@ -129,8 +129,10 @@ int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v
  *   tokens [batch, B] int32, conf [batch, B] fp32, n_commit [batch] int32 (written)
  *   workspace        device buffer of >= mars_accept_workspace_size(batch, B, V)
  *                    bytes.  It holds one partial result per 16 KB slice of
- *                    logits; its contents on entry do not matter.  Calls that
- *                    share a workspace must not overlap in time.
+ *                    logits (and, for the batch-minimum mode of mars_accept_ex,
+ *                    one count per sequence); its contents on entry do not
+ *                    matter.  Calls that share a workspace must not overlap in
+ *                    time.
  * The call is two kernel launches on `stream` (the streaming reduction, then
  * one CTA per sequence for the commit rule and the append).
  * If cache_len[b] + n > cap nothing is appended for b, cache_len[b] is kept,
@@ -144,6 +146,31 @@ int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau,
                 int Hkv, int D, int cap,
                 int32_t* tokens, float* conf, int32_t* n_commit,
                 int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mars_accept_ex - mars_accept with options, `flags` an OR of:
+ *   MARS_ACCEPT_MARGIN     conf is the margin p1 - p2 (see mars_accept_margin);
+ *   MARS_ACCEPT_BATCH_MIN  every sequence commits n = min over the batch of the
+ *                          per-sequence counts (each at least one) and appends n
+ *                          rows: the paper's original sampler, whose block-level
+ *                          cache advanced at the batch-minimum acceptance (the
+ *                          authors' MARS blog post, "Inference: a knob, not a mode
+ *                          switch").  n_commit[b] = n for every b; one more launch
+ *                          (one CTA per sequence) takes the minimum and appends.
+ *                          A sequence for which cache_len[b] + n > cap sets
+ *                          MARS_DEV_CAPACITY, commits 0 and is left unchanged.
+ * Other bits return MARS_ERR_INVALID_ARG.  Arguments, workspace (its size from
+ * mars_accept_workspace_size covers both modes) and outputs are those of
+ * mars_accept.  mars_accept(...) == mars_accept_ex(..., flags = 0, ...).
+ */
+#define MARS_ACCEPT_MARGIN 1
+#define MARS_ACCEPT_BATCH_MIN 2
+int mars_accept_ex(const uint16_t* logits, int batch, int B, int V, float tau, int flags,
+                   const uint16_t* k_new, const uint16_t* v_new,
+                   uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
+                   int Hkv, int D, int cap,
+                   int32_t* tokens, float* conf, int32_t* n_commit,
+                   int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * mars_accept_margin - mars_accept with the margin gate.  The authors' MARS blog

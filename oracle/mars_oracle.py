@@ -32,7 +32,8 @@ Readings taken where the pages are silent:
   as p1 - p2, the top-1 probability minus the largest probability of any
   other token;
 * the block-level KV cache advances per sequence by that sequence's own
-  commit count (the batch-minimum variant is not part of this oracle).
+  commit count, or, in the batch-minimum mode of the paper's original
+  sampler, every sequence by the smallest count of the batch.
 
 Parity pins for every function live in ``tests/test_oracle_*.py``; no
 function here is unpinned.
@@ -223,10 +224,17 @@ def commit_count(conf_row, tau: float) -> int:
     return max(n, 1)
 
 
-def accept(logits, tau: float, gate: str = "prob"):
-    """tokens [b, B], conf [b, B], n_commit [b] for logits [b, B, V] (gate: see accept_rows)."""
+def accept(logits, tau: float, gate: str = "prob", batch_min: bool = False):
+    """tokens [b, B], conf [b, B], n_commit [b] for logits [b, B, V] (gate: see accept_rows).
+
+    batch_min: the paper's original sampler, whose block-level cache advanced at
+    the batch-minimum acceptance ([blog] "Inference"): every sequence commits the
+    smallest of the per-sequence counts.
+    """
     tokens, conf = accept_rows(logits, gate)
     n = np.array([commit_count(conf[b], tau) for b in range(conf.shape[0])], dtype=np.int64)
+    if batch_min:
+        n = np.full_like(n, n.min())
     return tokens, conf, n
 
 

@@ -414,6 +414,22 @@ def check_accept_tau_extremes(accept):
     assert np.all(n == 6)
 
 
+def check_batch_min(accept):
+    """Batch-minimum mode: every sequence commits the smallest per-sequence count."""
+    x = np.full((3, 4, 10), -5.0)
+    x[:, :, 0] = 5.0               # confident everywhere: conf = 1 / (1 + 9 e^-10) ~ 0.9996
+    x[1, 2, 0] = -5.0              # sequence 1: position 2 is uniform (conf 0.1)
+    x[2, 0, 0] = -5.0              # sequence 2: position 0 uniform -> at least one still commits
+    _, _, n = accept(x, 0.9)
+    assert list(n) == [4, 2, 1]
+    _, _, n = accept(x, 0.9, batch_min=True)
+    assert list(n) == [1, 1, 1]
+    _, _, n = accept(x[:2], 0.9, batch_min=True)
+    assert list(n) == [2, 2]
+    _, _, n = accept(x[:1], 0.9, batch_min=True)
+    assert list(n) == [4]
+
+
 def check_append(append_kv):
     nb, B, hkv, D, cap = 3, 4, 2, 5, 12
     kc, vc = rand((nb, hkv, cap, D), 41), rand((nb, hkv, cap, D), 42)

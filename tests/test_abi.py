@@ -26,7 +26,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "mars_accept", "mars_accept_margin", "mars_accept_noalloc", "mars_accept_workspace_size", "mars_decode_attn",
+        "mars_accept", "mars_accept_ex", "mars_accept_margin", "mars_accept_noalloc", "mars_accept_workspace_size", "mars_decode_attn",
         "mars_last_cuda_error", "mars_status_string", "mars_train_attn", "mars_version"])
 
 

@@ -103,3 +103,55 @@ def test_ragged_vocab(V):
     conf, _, _ = check_full(logits, 0.2, [5, 0, 17], seed=V)
     if V == 1:
         assert np.all(conf == 1.0)
+
+
+def run_batch_min(logits, tau, kn, vn, kc, vc, lens, gate="prob"):
+    d_kc, d_vc = dev_bf16(kc), dev_bf16(vc)
+    d_len = torch.from_numpy(np.asarray(lens, dtype=np.int32)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tok, conf, n = mars.accept(dev_bf16(logits), tau, dev_bf16(kn), dev_bf16(vn), d_kc, d_vc, d_len,
+                               status=status, gate=gate, batch_min=True)
+    torch.cuda.synchronize()
+    return (tok.cpu().numpy(), conf.cpu().numpy(), n.cpu().numpy(), bits_of(d_kc), bits_of(d_vc),
+            d_len.cpu().numpy(), int(status.item()))
+
+
+@pytest.mark.parametrize("gate", ["prob", "margin"])
+def test_batch_minimum_mode(gate):
+    """The paper's original sampler: every sequence commits the batch-minimum count."""
+    g = np.random.default_rng(21)
+    batch, B, V, hkv, D = 16, 8, 3000, 2, 64
+    x = g.standard_normal((batch, B, V), dtype=np.float32)
+    for b in range(batch):
+        for i in range(B):
+            x[b, i, g.integers(0, V)] += g.uniform(6.0, 16.0)
+    x[:, :2, 5] += 30.0  # the first two positions always pass: the minimum is at least 2
+    logits = synth.Bf16.from_float(x)
+    lens = g.integers(0, 50, size=batch).astype(np.int32)
+    kn, vn, kc, vc = kv_for(batch, B, hkv, D, 64, 22)
+    tok, conf, n, kc2, vc2, lens2, status = run_batch_min(logits, 0.2, kn, vn, kc, vc, lens, gate)
+    assert status == 0
+    t_o, c_o, n_o = oracle.accept(logits.f64, 0.2, gate, batch_min=True)
+    assert np.array_equal(tok, t_o)
+    _, _, n_each = oracle.accept(logits.f64, 0.2, gate)
+    assert len(set(n_each.tolist())) > 1  # the per-sequence counts differ, so the mode matters
+    assert np.all(n == n[0]) and np.array_equal(n, n_o) and n[0] >= 2, (n, n_o)
+    kc_o, vc_o, len_o = oracle.append_kv(kc.bits, vc.bits, lens, kn.bits, vn.bits, n_o)
+    assert np.array_equal(lens2, len_o) and np.array_equal(kc2, kc_o) and np.array_equal(vc2, vc_o)
+
+
+def test_batch_minimum_mode_capacity():
+    """A sequence without room for the batch-minimum count reports and keeps its cache."""
+    g = np.random.default_rng(23)
+    batch, B, V, hkv, D, cap = 4, 4, 500, 1, 64, 16
+    x = g.standard_normal((batch, B, V), dtype=np.float32)
+    x[:, :, 7] += 20.0  # every position confident: counts are B everywhere
+    logits = synth.Bf16.from_float(x)
+    lens = np.array([0, 5, 14, 12], dtype=np.int32)  # 14 + 4 > 16
+    kn, vn, kc, vc = kv_for(batch, B, hkv, D, cap, 24)
+    tok, conf, n, kc2, vc2, lens2, status = run_batch_min(logits, 0.5, kn, vn, kc, vc, lens)
+    assert status & mars.MARS_DEV_CAPACITY
+    assert list(n) == [4, 4, 0, 4]
+    n_eff = np.array([4, 4, 0, 4])
+    kc_o, vc_o, len_o = oracle.append_kv(kc.bits, vc.bits, lens, kn.bits, vn.bits, n_eff)
+    assert np.array_equal(lens2, len_o) and np.array_equal(kc2, kc_o) and np.array_equal(vc2, vc_o)

@@ -47,6 +47,7 @@ def all_pins(m):
         "commit": lambda: pins.check_commit_rule(m.commit_count),
         "tau": lambda: pins.check_accept_tau_extremes(m.accept),
         "append": lambda: pins.check_append(m.append_kv),
+        "batch_min": lambda: pins.check_batch_min(m.accept),
     }
     failed = []
     for name, fn in checks.items():
@@ -93,6 +94,8 @@ MUTATIONS = [
     ("(others.max() if others.size else 0.0)", "(others.max() if others.size else p[tok])"),
     # margin: unnormalised (logit-domain) difference
     ("            p /= p.sum()\n", ""),
+    # batch-minimum mode taking the maximum
+    ("n = np.full_like(n, n.min())", "n = np.full_like(n, n.max())"),
     # strict > instead of >= tau
     ("if c >= tau:", "if c > tau:"),
     # the at-least-one rule dropped

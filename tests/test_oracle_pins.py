@@ -117,6 +117,10 @@ def test_accept_tau_extremes():
     pins.check_accept_tau_extremes(oracle.accept)
 
 
+def test_batch_min_mode():
+    pins.check_batch_min(oracle.accept)
+
+
 def test_append():
     pins.check_append(oracle.append_kv)
 

@@ -22,6 +22,10 @@ MARS_ERR_INVALID_ARG = 1
 MARS_ERR_WORKSPACE_TOO_SMALL = 2
 MARS_ERR_CUDA = 3
 MARS_ERR_UNSUPPORTED_DEVICE = 4
+MARS_ERR_SCRATCH_LIMIT = 5
+
+MARS_ACCEPT_MARGIN = 1
+MARS_ACCEPT_BATCH_MIN = 2
 
 MARS_DEV_CAPACITY = 1
 MARS_DEV_LEN_RANGE = 2
@@ -41,6 +45,7 @@ _SIGNATURES = {
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
     "mars_accept": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_margin": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "mars_accept_ex": (_I, [_P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_noalloc": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
 }
 
@@ -189,11 +194,12 @@ def accept_workspace(batch: int, B: int, V: int, device) -> torch.Tensor:
 
 
 def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, workspace=None, tokens=None, conf=None,
-           n_commit=None, status=None, stream=None, gate: str = "prob"):
+           n_commit=None, status=None, stream=None, gate: str = "prob", batch_min: bool = False):
     """Greedy tokens, confidences, left-to-right commit and KV append
-    (include/mars.h: mars_accept, or mars_accept_margin with gate="margin", where
-    conf is p1 - p2).  Returns (tokens, conf, n_commit); k_cache, v_cache and
-    cache_len are updated in place."""
+    (include/mars.h: mars_accept_ex; gate="margin" makes conf p1 - p2,
+    batch_min=True commits the batch-minimum count for every sequence).
+    Returns (tokens, conf, n_commit); k_cache, v_cache and cache_len are
+    updated in place."""
     if gate not in ("prob", "margin"):
         raise ValueError(f"gate must be 'prob' or 'margin', got {gate!r}")
     nb, bq, V = logits.shape
@@ -219,9 +225,10 @@ def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, worksp
     _check(n_commit, "n_commit", torch.int32, (nb,), dev)
     if status is not None:
         _check(status, "status", torch.int32, (1,), dev)
-    _call("mars_accept_margin" if gate == "margin" else "mars_accept", _ptr(logits), nb, bq, V, float(tau),
-          _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens),
-          _ptr(conf), _ptr(n_commit), _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream))
+    flags = (MARS_ACCEPT_MARGIN if gate == "margin" else 0) | (MARS_ACCEPT_BATCH_MIN if batch_min else 0)
+    _call("mars_accept_ex", _ptr(logits), nb, bq, V, float(tau), flags, _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+          _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
+          _ptr(workspace), workspace.numel(), _stream(stream))
     return tokens, conf, n_commit
 
 

@@ -151,7 +151,9 @@ struct AcceptArgs {
   int32_t* n_commit;
   int32_t* status;
   int margin;           // 1: conf = p1 - p2 (margin gate); 0: conf = p1
+  int batch_min;        // 1: every sequence commits the batch minimum of the counts
   Partial* partials;    // [rows][chunks]
+  int32_t* counts;      // [batch] per-sequence counts (batch-minimum mode), after the partials
   int chunks;           // chunks per row
   int items;            // rows * chunks
 };
@@ -223,6 +225,11 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
   if (warp == 0) {
     const bool pass = lane < a.B && s_conf[min(lane, a.B - 1)] >= a.tau;
     const uint32_t ok = __ballot_sync(0xffffffffu, pass);
+    if (a.batch_min) {
+      // the batch-minimum launch that follows commits and appends
+      if (lane == 0) a.counts[b] = max(min(__ffs(~ok) - 1, a.B), 1);
+      return;
+    }
     if (lane == 0) {
       int n = max(min(__ffs(~ok) - 1, a.B), 1);
       if (len0 < 0 || len0 + n > a.cap) {
@@ -234,6 +241,7 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
       a.cache_len[b] = len0 + n;
     }
   }
+  if (a.batch_min) return;
   __syncthreads();
   // ---- block-level KV append of the committed rows: candidate vector e is
   // (position i, head g, chunk c) with e = (i * Hkv + g) * vec_per_row + c
@@ -385,11 +393,54 @@ inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b -
 // Chunks per row of V logits (a row's aligned part has at most ceil(V/8) vectors).
 inline int chunks_for(int V) { return max(1, ceil_div(ceil_div(V, 8), kChunkVec)); }
 
+// Batch-minimum mode (the paper's original sampler: the block-level cache of a
+// batch advances at its minimum acceptance): one CTA per sequence commits
+// n = min over the batch of the per-sequence counts and appends n rows.
+__global__ void __launch_bounds__(256) accept_batchmin_kernel(const AcceptArgs a) {
+  __shared__ int s_min[8];
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int len0 = __ldg(a.cache_len + b);
+  griddep_wait();  // the per-sequence counts are complete and visible from here on
+  int m = a.B;
+  for (int t = threadIdx.x; t < a.batch; t += blockDim.x) m = min(m, __ldcg(a.counts + t));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) s_min[warp] = m;
+  __syncthreads();
+  int n = s_min[0];
+  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) n = min(n, s_min[w]);
+  if (len0 < 0 || len0 + n > a.cap) {
+    if (threadIdx.x == 0) {
+      set_status(a.status, MARS_DEV_CAPACITY);
+      a.n_commit[b] = 0;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    a.n_commit[b] = n;
+    a.cache_len[b] = len0 + n;
+  }
+  const int vec_per_row = a.D >> 3;
+  const int per_pos = a.Hkv * vec_per_row;
+  for (int e = threadIdx.x; e < n * per_pos; e += blockDim.x) {
+    const size_t src = (static_cast<size_t>(b) * a.B * per_pos + e) * 8;
+    const int i = e / per_pos, g = (e / vec_per_row) % a.Hkv, c = e % vec_per_row;
+    const size_t dst = ((static_cast<size_t>(b) * a.Hkv + g) * a.cap + len0 + i) * a.D + 8 * c;
+    *reinterpret_cast<uint4*>(a.k_cache + dst) = *reinterpret_cast<const uint4*>(a.k_new + src);
+    *reinterpret_cast<uint4*>(a.v_cache + dst) = *reinterpret_cast<const uint4*>(a.v_new + src);
+  }
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: one Partial per (row, chunk).
-inline size_t ws_bytes(int batch, int B, int V) {
+inline size_t partial_bytes(int batch, int B, int V) {
   return align_up(static_cast<size_t>(batch) * B * chunks_for(V) * sizeof(Partial), 256);
+}
+// Workspace: the partials, then one count per sequence (batch-minimum mode).
+inline size_t ws_bytes(int batch, int B, int V) {
+  return partial_bytes(batch, B, V) + align_up(static_cast<size_t>(batch) * sizeof(int32_t), 256);
 }
 
 int configure_kernel() {
@@ -431,7 +482,11 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_finish_kernel, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, accept_finish_kernel, a);
+  if (e != cudaSuccess || !a.batch_min) return e == cudaSuccess ? MARS_OK : mars_host::cuda_fail(e);
+  cfg.gridDim = dim3(a.batch, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, accept_batchmin_kernel, a);
   return e == cudaSuccess ? MARS_OK : mars_host::cuda_fail(e);
 }
 
@@ -478,7 +533,9 @@ AcceptArgs make_args(const uint16_t* logits, int batch, int B, int V, float tau,
   a.n_commit = n_commit;
   a.status = status;
   a.margin = 0;
+  a.batch_min = 0;
   a.partials = nullptr;
+  a.counts = nullptr;
   a.chunks = a.items = 0;
   return a;
 }
@@ -490,13 +547,15 @@ extern "C" size_t mars_accept_workspace_size(int batch, int B, int V) {
   return ws_bytes(batch, B, V);
 }
 
-extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
-                           const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len, int Hkv,
-                           int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit, int32_t* status,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" int mars_accept_ex(const uint16_t* logits, int batch, int B, int V, float tau, int flags,
+                              const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache,
+                              int32_t* cache_len, int Hkv, int D, int cap, int32_t* tokens, float* conf,
+                              int32_t* n_commit, int32_t* status, void* workspace, size_t workspace_bytes,
+                              void* stream) {
   int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
                       conf, n_commit, status);
   if (rc != MARS_OK) return rc;
+  MARS_HOST_CHECK((flags & ~(MARS_ACCEPT_MARGIN | MARS_ACCEPT_BATCH_MIN)) == 0, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(workspace != nullptr && mars_host::aligned16(workspace), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(workspace_bytes >= ws_bytes(batch, B, V), MARS_ERR_WORKSPACE_TOO_SMALL);
   rc = mars_host::check_device();
@@ -504,27 +563,27 @@ extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, floa
 
   AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
                            conf, n_commit, status);
+  a.margin = (flags & MARS_ACCEPT_MARGIN) ? 1 : 0;
+  a.batch_min = (flags & MARS_ACCEPT_BATCH_MIN) ? 1 : 0;
   a.partials = static_cast<Partial*>(workspace);
+  a.counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + partial_bytes(batch, B, V));
   return launch(a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
+                           const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len, int Hkv,
+                           int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit, int32_t* status,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return mars_accept_ex(logits, batch, B, V, tau, 0, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                        conf, n_commit, status, workspace, workspace_bytes, stream);
 }
 
 extern "C" int mars_accept_margin(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
                                   const uint16_t* v_new, uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
                                   int Hkv, int D, int cap, int32_t* tokens, float* conf, int32_t* n_commit,
                                   int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
-                      conf, n_commit, status);
-  if (rc != MARS_OK) return rc;
-  MARS_HOST_CHECK(workspace != nullptr && mars_host::aligned16(workspace), MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(workspace_bytes >= ws_bytes(batch, B, V), MARS_ERR_WORKSPACE_TOO_SMALL);
-  rc = mars_host::check_device();
-  if (rc != MARS_OK) return rc;
-
-  AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
-                           conf, n_commit, status);
-  a.margin = 1;
-  a.partials = static_cast<Partial*>(workspace);
-  return launch(a, static_cast<cudaStream_t>(stream));
+  return mars_accept_ex(logits, batch, B, V, tau, MARS_ACCEPT_MARGIN, k_new, v_new, k_cache, v_cache, cache_len, Hkv,
+                        D, cap, tokens, conf, n_commit, status, workspace, workspace_bytes, stream);
 }
 
 // ============================================================================
