@@ -49,10 +49,12 @@ __all__ = [
     "mars_mask",
     "train_attn",
     "decode_attn",
+    "decode_attn_deferred",
     "accept_rows",
     "commit_count",
     "accept",
     "append_kv",
+    "accept_deferred",
     "near_threshold",
 ]
 
@@ -171,6 +173,63 @@ def decode_attn(q, k_new, v_new, k_cache, v_cache, cache_len, scale: float):
             scores = scale * (q[b, :, h, :] @ keys.T)
             out[b, :, h, :], _ = _softmax_attend(scores, visible, vals)
     return out
+
+
+def decode_attn_deferred(q, k_new, v_new, k_cache, v_cache, cache_len, pending, scale: float):
+    """One decode step of the deferred-KV sampler ([blog] "Inference": KV
+    commitment deferred into the next proposal forward, per-sample cursors and
+    a cache-validity bitmask).
+
+    The forward of step t carries, per sequence b, 2B slots: slots 0..B-1 hold
+    the tokens committed at step t-1 (valid while slot < pending[b]; their K/V
+    are computed by this forward, so no extra forward recomputes them) and
+    slots B..2B-1 the B new [MASK] placeholders.  q: [b, 2B, Hq, D]; k_new,
+    v_new: [b, 2B, Hkv, D].  The valid slots follow the cache_len[b] committed
+    cache rows in slot order; a valid query slot sees every cache row and the
+    valid slots up to itself.  The valid pending rows are written into the cache
+    at cache_len[b] .. cache_len[b] + pending[b] - 1 (cache_len itself is
+    advanced by the acceptance step).
+
+    Returns (o [b, 2B, Hq, D] with zero rows at invalid slots, k_cache', v_cache')
+    where the caches are updated copies.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    nb, s2, hq, d = q.shape
+    B = s2 // 2
+    hkv = k_new.shape[2]
+    group = hq // hkv
+    out = np.zeros_like(q)
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    for b in range(nb):
+        n, p = int(cache_len[b]), int(pending[b])
+        slots = list(range(p)) + list(range(B, 2 * B))  # valid slots in position order
+        for g in range(hkv):
+            kc[b, g, n:n + p, :] = k_new[b, :p, g, :]
+            vc[b, g, n:n + p, :] = v_new[b, :p, g, :]
+        for h in range(hq):
+            g = h // group
+            keys = np.concatenate([k_cache[b, g, :n, :], k_new[b, slots, g, :]], axis=0)
+            vals = np.concatenate([v_cache[b, g, :n, :], v_new[b, slots, g, :]], axis=0)
+            nq = len(slots)
+            visible = np.ones((nq, n + nq), dtype=bool)
+            for j in range(nq):
+                visible[j, n + j + 1:] = False
+            scores = scale * (q[b, slots, h, :] @ keys.T)
+            out[b, slots, h, :], _ = _softmax_attend(scores, visible, vals)
+    return out, kc, vc
+
+
+def accept_deferred(logits, tau: float, cache_len, pending, gate: str = "prob"):
+    """Acceptance step of the deferred-KV sampler: the same tokens, confidences
+    and commit counts as accept(), but no K/V is copied; the cursor advances by
+    the previous step's count (the rows the decode step just wrote) and the new
+    count becomes the pending count of the next step.
+
+    Returns (tokens, conf, n_new, cache_len') with cache_len' = cache_len + pending.
+    """
+    tokens, conf, n = accept(logits, tau, gate)
+    return tokens, conf, n, np.asarray(cache_len, dtype=np.int64) + np.asarray(pending, dtype=np.int64)
 
 
 # --------------------------------------------------------------------------

@@ -430,6 +430,63 @@ def check_batch_min(accept):
     assert list(n) == [4]
 
 
+def _deferred_case(seed, nb=3, B=4, hq=4, hkv=2, D=8, cap=40):
+    q = rand((nb, 2 * B, hq, D), seed)
+    kn, vn = rand((nb, 2 * B, hkv, D), seed + 1), rand((nb, 2 * B, hkv, D), seed + 2)
+    kc, vc = rand((nb, hkv, cap, D), seed + 3), rand((nb, hkv, cap, D), seed + 4)
+    return q, kn, vn, kc, vc
+
+
+def check_deferred_matches_append_then_decode(decode_attn_deferred, decode_attn, append_kv):
+    """Deferred step = (append the pending rows, then an ordinary decode step of the masks)
+    for the mask slots; the cache ends with the pending rows written."""
+    B = 4
+    q, kn, vn, kc, vc = _deferred_case(46, B=B)
+    lens, pend = np.array([5, 0, 11]), np.array([2, 4, 0])
+    o, kc2, vc2 = decode_attn_deferred(q, kn, vn, kc, vc, lens, pend, 0.35)
+    kc_a, vc_a, len_a = append_kv(kc, vc, lens, kn[:, :B], vn[:, :B], pend)
+    o_ref = decode_attn(q[:, B:], kn[:, B:], vn[:, B:], kc_a, vc_a, len_a, 0.35)
+    assert np.allclose(o[:, B:], o_ref, rtol=0, atol=1e-13)
+    assert np.array_equal(kc2, kc_a) and np.array_equal(vc2, vc_a)
+
+
+def check_deferred_pending_rows_are_causal(decode_attn_deferred, train_attn):
+    """With an empty cache the valid pending slots are plain causal attention over
+    themselves: the clean half of training attention for L = pending."""
+    B, p = 4, 3
+    q, kn, vn, kc, vc = _deferred_case(47, nb=1, B=B, hq=2, hkv=1)
+    o, _, _ = decode_attn_deferred(q, kn, vn, kc, vc, np.array([0]), np.array([p]), 0.5)
+    zq = np.concatenate([q[:, :p], q[:, :p]], axis=1)     # [x ; x~] with x~ unused here
+    zk = np.concatenate([kn[:, :p], kn[:, :p]], axis=1)
+    zv = np.concatenate([vn[:, :p], vn[:, :p]], axis=1)
+    ot, _ = train_attn(zq, zk, zv, p, 1, 0.5, rows=range(p))
+    assert np.allclose(o[:, :p], ot[:, :p], rtol=0, atol=1e-13)
+
+
+def check_deferred_invalid_slots(decode_attn_deferred):
+    """Invalid pending slots give zero rows and never reach a valid row, even as NaN."""
+    B = 4
+    q, kn, vn, kc, vc = _deferred_case(48, B=B)
+    lens, pend = np.array([3, 7, 1]), np.array([1, 0, 3])
+    o1, _, _ = decode_attn_deferred(q, kn, vn, kc, vc, lens, pend, 0.35)
+    for b, p in enumerate(pend):
+        q[b, p:B] = np.nan
+        kn[b, p:B] = np.nan
+        vn[b, p:B] = np.nan
+    o2, kc2, _ = decode_attn_deferred(q, kn, vn, kc, vc, lens, pend, 0.35)
+    assert np.array_equal(o1, o2) and np.all(np.isfinite(kc2))
+    for b, p in enumerate(pend):
+        assert np.all(o2[b, p:B] == 0)
+
+
+def check_accept_deferred(accept_deferred, accept):
+    x = rand((3, 4, 50), 49, sigma=3.0)
+    tok, conf, n, ln = accept_deferred(x, 0.5, np.array([4, 0, 9]), np.array([2, 0, 3]))
+    t2, c2, n2 = accept(x, 0.5)
+    assert np.array_equal(tok, t2) and np.array_equal(conf, c2) and np.array_equal(n, n2)
+    assert list(ln) == [6, 0, 12]
+
+
 def check_append(append_kv):
     nb, B, hkv, D, cap = 3, 4, 2, 5, 12
     kc, vc = rand((nb, hkv, cap, D), 41), rand((nb, hkv, cap, D), 42)

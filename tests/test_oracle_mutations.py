@@ -48,6 +48,11 @@ def all_pins(m):
         "tau": lambda: pins.check_accept_tau_extremes(m.accept),
         "append": lambda: pins.check_append(m.append_kv),
         "batch_min": lambda: pins.check_batch_min(m.accept),
+        "deferred_eq": lambda: pins.check_deferred_matches_append_then_decode(m.decode_attn_deferred, m.decode_attn,
+                                                                              m.append_kv),
+        "deferred_causal": lambda: pins.check_deferred_pending_rows_are_causal(m.decode_attn_deferred, m.train_attn),
+        "deferred_invalid": lambda: pins.check_deferred_invalid_slots(m.decode_attn_deferred),
+        "accept_deferred": lambda: pins.check_accept_deferred(m.accept_deferred, m.accept),
     }
     failed = []
     for name, fn in checks.items():
@@ -80,7 +85,11 @@ MUTATIONS = [
     # placeholders see each other bidirectionally in decode
     ("visible[i, n + i + 1:] = False", "pass"),
     # decode reads the wrong KV head
-    ("            g = h // group\n            keys =", "            g = 0\n            keys ="),
+    ("            g = h // group\n            keys = np.concatenate([k_cache[b, g, :n, :], k_new[b, :, g, :]]",
+     "            g = 0\n            keys = np.concatenate([k_cache[b, g, :n, :], k_new[b, :, g, :]]"),
+    # deferred decode reads the wrong KV head
+    ("            g = h // group\n            keys = np.concatenate([k_cache[b, g, :n, :], k_new[b, slots, g, :]]",
+     "            g = 0\n            keys = np.concatenate([k_cache[b, g, :n, :], k_new[b, slots, g, :]]"),
     # argmax ties go to the last index
     ("tok = int(np.flatnonzero(row == m)[0])", "tok = int(np.flatnonzero(row == m)[-1])"),
     # confidence taken as the sum instead of its inverse
@@ -94,6 +103,16 @@ MUTATIONS = [
     ("(others.max() if others.size else 0.0)", "(others.max() if others.size else p[tok])"),
     # margin: unnormalised (logit-domain) difference
     ("            p /= p.sum()\n", ""),
+    # deferred: the masks do not see the pending rows
+    ("        slots = list(range(p)) + list(range(B, 2 * B))  # valid slots in position order",
+     "        slots = list(range(B, 2 * B)) + list(range(p))"),
+    # deferred: invalid pending slots treated as valid
+    ("list(range(p)) + list(range(B, 2 * B))", "list(range(2 * B))"),
+    # deferred: pending rows written one slot too far
+    ("            kc[b, g, n:n + p, :] = k_new[b, :p, g, :]", "            kc[b, g, n + 1:n + p + 1, :] = k_new[b, :p, g, :]"),
+    # deferred acceptance advancing by the new count instead of the pending one
+    ("np.asarray(cache_len, dtype=np.int64) + np.asarray(pending, dtype=np.int64)",
+     "np.asarray(cache_len, dtype=np.int64) + n"),
     # batch-minimum mode taking the maximum
     ("n = np.full_like(n, n.min())", "n = np.full_like(n, n.max())"),
     # strict > instead of >= tau

@@ -121,6 +121,22 @@ def test_batch_min_mode():
     pins.check_batch_min(oracle.accept)
 
 
+def test_deferred_matches_append_then_decode():
+    pins.check_deferred_matches_append_then_decode(oracle.decode_attn_deferred, oracle.decode_attn, oracle.append_kv)
+
+
+def test_deferred_pending_rows_are_causal():
+    pins.check_deferred_pending_rows_are_causal(oracle.decode_attn_deferred, oracle.train_attn)
+
+
+def test_deferred_invalid_slots():
+    pins.check_deferred_invalid_slots(oracle.decode_attn_deferred)
+
+
+def test_accept_deferred():
+    pins.check_accept_deferred(oracle.accept_deferred, oracle.accept)
+
+
 def test_append():
     pins.check_append(oracle.append_kv)
 
