@@ -18,6 +18,7 @@ on bounded samples of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -126,9 +127,13 @@ def sum_over_ranks(dist, world, value, device):
 # --------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock and throttle reasons; only the samples whose
+    timestamps fall inside the timed window (host wall clock) are reported."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -143,11 +148,21 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.PERIOD_MS)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        # the window opens only once the sampler is producing lines
+        t0 = time.time()
+        while time.time() - t0 < 10 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
-    def stop(self):
+    def stop(self, window):
+        """window = (start, end) as datetime.datetime on the host clock."""
+        import datetime
+
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -156,25 +171,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
+        outside = 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    mhz, max_mhz = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[5:9]):
+                if not window[0] <= ts <= window[1]:
+                    outside += 1
+                    continue
+                sm.append(mhz)
+                smax.append(max_mhz)
+                for name, val in zip(names, parts[6:10]):
                     if val.lower().startswith("active"):
                         reasons.add(name)
         os.unlink(self.path)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "samples_outside": outside,
+                    "reasons": ["no samples in the timed window"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "period_ms": self.PERIOD_MS, "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------------------
@@ -352,6 +374,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
+    win0 = datetime.datetime.now()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -359,7 +382,7 @@ def run_gpu(args, rank, world, local):
         step(args.warmup + k, events[k])
     t_end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop((win0, datetime.datetime.now()))
     barrier(dist, world)
     total_ms = t_start.elapsed_time(t_end)
     per_kernel_ms = {n: [events[k][j].elapsed_time(events[k][j + 1]) for k in range(args.steps)]
@@ -428,6 +451,9 @@ def run_gpu(args, rank, world, local):
                                                     "accept_margin_b64", gate="margin")
     parts["accept_batchmin_b64"] = run_accept_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic,
                                                       "accept_batchmin_b64", batch_min=True)
+    # the deferred-KV sampler (decode over 2B slots with the fused commit, then the
+    # acceptance that only moves the cursor), timed the same way
+    parts.update(run_deferred_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic, gen))
 
     line = {
         "metric": METRIC,
@@ -523,6 +549,73 @@ def run_accept_variant(args, mars, work, device, hbm_peak, traffic, name, gate="
     work.reset()
     return {"avg_us": round(ms / n * 1e3, 3), "calls": n,
             "roofline": roofline("hbm", achieved, hbm_peak, "GB/s", traffic.get(name))}
+
+
+def run_deferred_variant(args, mars, work, device, hbm_peak, traffic, gen):
+    """The deferred-KV sampler on the batch-64 decode workload: min(steps, 64) steps
+    after a cache reset, each step the deferred decode step (2B slots: the previous
+    step's committed tokens, then B placeholders) and the deferred acceptance, every
+    launch bracketed by CUDA events on the stream."""
+    import torch
+
+    s = work.s
+    n = max(1, min(args.steps, 64))
+    total = args.warmup + n
+    stream = torch.cuda.current_stream()
+    q2 = torch.randn((s.batch, 2 * s.B, s.Hq, s.D), generator=gen, device=device).to(torch.bfloat16)
+    kn2 = torch.randn((s.batch, 2 * s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+    vn2 = torch.randn((s.batch, 2 * s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+    o2 = torch.empty_like(q2)
+    pend = [torch.zeros((s.batch,), dtype=torch.int32, device=device) for _ in range(work.nsets)]
+    hist_len = torch.zeros((total, s.batch), dtype=torch.int32, device=device)
+    hist_p = torch.zeros((total, s.batch), dtype=torch.int32, device=device)
+    hist_n = torch.zeros((total, s.batch), dtype=torch.int32, device=device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+
+    def call(i, e=None):
+        st, p = work.sets[i % work.nsets], pend[i % work.nsets]
+        hist_len[i].copy_(st["lens"])
+        hist_p[i].copy_(p)
+        if e is not None:
+            e[0].record(stream)
+        mars.decode_attn_deferred(q2, kn2, vn2, st["kc"], st["vc"], st["lens"], p, work.max_len, o=o2)
+        if e is not None:
+            e[1].record(stream)
+        mars.accept_deferred(st["logits"], DECODE_TAU, st["lens"], p, s.cap, workspace=st["ws"],
+                             tokens=work.tokens, conf=work.conf)
+        if e is not None:
+            e[2].record(stream)
+        hist_n[i].copy_(p)  # this step's count (the next step's pending)
+
+    work.reset()
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    for i in range(n):
+        call(args.warmup + i, ev[i])
+    torch.cuda.synchronize()
+    dec_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    acc_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    lens = hist_len[args.warmup:].to(torch.int64).sum(dim=1).cpu().numpy()
+    pends = hist_p[args.warmup:].to(torch.int64).sum(dim=1).cpu().numpy()
+    kv_row = s.Hkv * s.D * 2 * 2  # K and V bytes of one cache row
+    dec_bytes = int((lens * kv_row).sum()) + n * s.batch * 2 * s.B * (2 * s.Hkv + 2 * s.Hq) * s.D * 2 \
+        + int((pends * kv_row).sum())
+    acc_bytes = n * (s.batch * s.B * s.V * 2 + s.batch * s.B * 8 + s.batch * 16)
+    committed = float(hist_n[args.warmup:].to(torch.float64).sum(dim=1).mean().item())
+    work.reset()
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    acc_gbs = acc_bytes / (acc_ms * 1e-3) / 1e9
+    return {
+        "decode_attn_deferred_b64": {"avg_us": round(dec_ms / n * 1e3, 3), "calls": n,
+                                     "roofline": roofline("hbm", dec_gbs, hbm_peak, "GB/s",
+                                                          traffic.get("decode_attn_deferred_b64"))},
+        "accept_deferred_b64": {"avg_us": round(acc_ms / n * 1e3, 3), "calls": n,
+                                "roofline": roofline("hbm", acc_gbs, hbm_peak, "GB/s",
+                                                     traffic.get("accept_deferred_b64"))},
+        "deferred_step_b64": {"steps_per_s": round(n / ((dec_ms + acc_ms) * 1e-3), 1),
+                              "tokens_per_step": round(committed, 3)},
+    }
 
 
 def run_b1_graph(args, mars, work, device):
@@ -650,7 +743,27 @@ def run_profile(args):
         shape = synth.DECODE_7B_B64 if part.endswith("b64") else synth.DECODE_7B_B1
         w = DecodeWork(shape, device, gen, 0, steps_per_episode=shape.steps)
         n_out = torch.zeros((shape.batch,), dtype=torch.int32, device=device)
-        if part.startswith("decode"):
+        s = shape
+        if "deferred" in part:
+            # a fixed pending count per sequence (uniform in [0, B]), restored before each call
+            pend0 = torch.randint(0, s.B + 1, (s.batch,), generator=gen, device=device, dtype=torch.int32)
+        if part == "decode_attn_deferred_b64":
+            q2 = torch.randn((s.batch, 2 * s.B, s.Hq, s.D), generator=gen, device=device).to(torch.bfloat16)
+            kn2 = torch.randn((s.batch, 2 * s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+            vn2 = torch.randn((s.batch, 2 * s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+            o2 = torch.empty_like(q2)
+
+            def run(i):
+                st = w.sets[i % w.nsets]
+                mars.decode_attn_deferred(q2, kn2, vn2, st["kc"], st["vc"], st["lens"], pend0, w.max_len, o=o2)
+        elif part == "accept_deferred_b64":
+            def run(i):
+                w.reset()
+                n_out.copy_(pend0)
+                st = w.sets[i % w.nsets]
+                mars.accept_deferred(st["logits"], DECODE_TAU, st["lens"], n_out, s.cap, workspace=st["ws"],
+                                     tokens=w.tokens, conf=w.conf)
+        elif part.startswith("decode"):
             run = lambda i: w.run_decode(mars, i)  # noqa: E731
         else:
             gate = "margin" if "margin" in part else "prob"
@@ -667,16 +780,21 @@ def run_profile(args):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: 1000 for the GPU arm, about half a second of GPU time; 10 for "
+                        "--impl reference)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["mars", "reference"], default="mars")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph batch-1 decode loop")
     p.add_argument("--profile", choices=["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1",
-                                         "accept_b1", "accept_margin_b64"],
+                                         "accept_b1", "accept_margin_b64", "decode_attn_deferred_b64",
+                                         "accept_deferred_b64"],
                    help="only launch this kernel, warm-up + steps times, and print no JSON (for ncu)")
     args = p.parse_args()
+    if args.steps is None:
+        args.steps = 10 if args.impl == "reference" else (3 if args.profile else 1000)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
     if args.profile:

@@ -46,7 +46,8 @@ extern "C" {
 #define MARS_ERR_SCRATCH_LIMIT 5       /* shape too large for mars_accept_noalloc's fixed scratch */
 
 /* Bits that kernels OR into the device status word. */
-#define MARS_DEV_CAPACITY 1   /* mars_accept: cache_len + n_commit would exceed cap; that sequence was not appended */
+#define MARS_DEV_CAPACITY 1   /* mars_accept: cache_len + n_commit would exceed cap; that sequence was not appended;
+                                 mars_decode_attn_deferred: cache_len + pending > cap; that sequence's output is zero */
 #define MARS_DEV_LEN_RANGE 2  /* mars_decode_attn: a cache_len[b] was < 0 or > max_len; that sequence's output is zero */
 #define MARS_DEV_TIMEOUT 4    /* mars_train_attn: an internal pipeline wait hit its iteration limit; output incomplete */
 
@@ -109,6 +110,44 @@ int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v
                      float scale, uint16_t* o, int32_t* status, void* stream);
 
 /*
+ * mars_decode_attn_deferred - the decode step of the deferred-KV sampler (the
+ * authors' MARS blog post, "Inference: a knob, not a mode switch": KV
+ * commitment is deferred into the next proposal forward, with per-sample
+ * cursors and a cache-validity bitmask, so that no extra forward, cache copy
+ * or batch-wide barrier commits the accepted tokens).
+ *
+ * The forward of this step carries S = 2B slots per sequence.  Slots 0..B-1
+ * hold the tokens that the previous step committed, fed back as ordinary
+ * tokens; slot c is valid while c < pending[b] (the previous step's n_commit).
+ * Slots B..2B-1 hold the B new [MASK] placeholders and are always valid.  The
+ * valid slots follow the cache_len[b] committed cache rows in slot order:
+ * a valid query slot sees every committed cache row and the valid slots up to
+ * and including itself (causal, as in the noisy intra-block case of Eq. 2).
+ * The output row of an invalid slot is zero, and nothing an invalid slot holds
+ * (even NaN) reaches a valid row.  The K/V rows of the valid pending slots are
+ * written into the cache at rows cache_len[b] .. cache_len[b] + pending[b] - 1;
+ * cache_len itself is advanced by mars_accept_ex with MARS_ACCEPT_DEFERRED.
+ *
+ *   q              [batch, 2B, Hq, D]     bf16
+ *   k_new, v_new   [batch, 2B, Hkv, D]    bf16  (K/V of this step's 2B slots)
+ *   k_cache, v_cache [batch, Hkv, cap, D] bf16  (read; the pending rows written)
+ *   cache_len      [batch] int32, device; every value in [0, max_len]
+ *   pending        [batch] int32, device; every value in [0, B]
+ *   o              [batch, 2B, Hq, D]     bf16 (written)
+ * Supported: D in {64, 128}; 1 <= B <= 8; Hq % Hkv == 0; max_len <= cap.
+ * A cache_len outside [0, max_len] or a pending outside [0, B] sets
+ * MARS_DEV_LEN_RANGE, and cache_len + pending > cap sets MARS_DEV_CAPACITY;
+ * either way that sequence's output is written as zeros and its cache is not
+ * written.  Other CTAs of the same sequence may read the rows being written
+ * inside their last cache tile; those rows are masked.  No workspace.
+ */
+int mars_decode_attn_deferred(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                              uint16_t* k_cache, uint16_t* v_cache,
+                              const int32_t* cache_len, const int32_t* pending,
+                              int batch, int B, int Hq, int Hkv, int D, int cap, int max_len,
+                              float scale, uint16_t* o, int32_t* status, void* stream);
+
+/*
  * mars_accept - confidence-threshold acceptance with the block-level KV
  * append ([blog] "Inference: a knob, not a mode switch": commit left to right
  * while the top-1 probability holds, stop at the first position below tau;
@@ -153,18 +192,33 @@ int mars_accept(const uint16_t* logits, int batch, int B, int V, float tau,
  *   MARS_ACCEPT_BATCH_MIN  every sequence commits n = min over the batch of the
  *                          per-sequence counts (each at least one) and appends n
  *                          rows: the paper's original sampler, whose block-level
- *                          cache advanced at the batch-minimum acceptance (the
- *                          authors' MARS blog post, "Inference: a knob, not a mode
- *                          switch").  n_commit[b] = n for every b; one more launch
+ *                          cache moved forward by the smallest acceptance in the
+ *                          batch (the authors' MARS blog post, "Inference: a knob,
+ *                          not a mode switch").  n_commit[b] = n for every b; one more launch
  *                          (one CTA per sequence) takes the minimum and appends.
  *                          A sequence for which cache_len[b] + n > cap sets
  *                          MARS_DEV_CAPACITY, commits 0 and is left unchanged.
+ *   MARS_ACCEPT_DEFERRED   the acceptance step of the deferred-KV sampler (see
+ *                          mars_decode_attn_deferred): on entry n_commit[b] holds
+ *                          the previous step's count, whose rows this step's
+ *                          decode attention has written at the cursor; the call
+ *                          sets cache_len[b] += that count, then n_commit[b] =
+ *                          this step's count (the next step's pending).  No K/V
+ *                          is copied: k_new, v_new, k_cache, v_cache, Hkv and D
+ *                          are not read and may be NULL / 0.  Tokens and conf
+ *                          are those of the other modes.  If the old count is
+ *                          outside [0, B] or cache_len + count > cap, the call
+ *                          sets MARS_DEV_CAPACITY, keeps cache_len and commits 0;
+ *                          if the new count would not fit after the cursor
+ *                          (cache_len + count > cap) it commits 0 and sets
+ *                          MARS_DEV_CAPACITY.  Combines with the other flags.
  * Other bits return MARS_ERR_INVALID_ARG.  Arguments, workspace (its size from
  * mars_accept_workspace_size covers both modes) and outputs are those of
  * mars_accept.  mars_accept(...) == mars_accept_ex(..., flags = 0, ...).
  */
 #define MARS_ACCEPT_MARGIN 1
 #define MARS_ACCEPT_BATCH_MIN 2
+#define MARS_ACCEPT_DEFERRED 4
 int mars_accept_ex(const uint16_t* logits, int batch, int B, int V, float tau, int flags,
                    const uint16_t* k_new, const uint16_t* v_new,
                    uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
@@ -174,9 +228,9 @@ int mars_accept_ex(const uint16_t* logits, int batch, int B, int V, float tau, i
 
 /*
  * mars_accept_margin - mars_accept with the margin gate.  The authors' MARS blog
- * post ("Inference: a knob, not a mode switch") reports that gating on how far
- * ahead the top token is, rather than on its probability, holds up better on
- * format-heavy text.  The margin is read as p1 - p2: the top-1 probability
+ * post ("Inference: a knob, not a mode switch") reports that a gate on the top
+ * token's lead over the rest, instead of on its probability, does better on
+ * text with strict formatting.  The margin is read as p1 - p2: the top-1 probability
  * minus the largest probability of any other token, at temperature 1.
  *
  * Same arguments, workspace, outputs and error behaviour as mars_accept,

@@ -28,7 +28,7 @@ Readings taken where the pages are silent:
 * L need not be a multiple of B: ceil() makes the last block short;
 * confidence = top-1 softmax probability at temperature 1; a position passes
   when conf >= tau; ties in the argmax go to the lowest vocabulary index;
-* the margin gate ([blog] "Inference": how far ahead the top token is) is read
+* the margin gate ([blog] "Inference": the top token's lead over the rest) is read
   as p1 - p2, the top-1 probability minus the largest probability of any
   other token;
 * the block-level KV cache advances per sequence by that sequence's own
@@ -243,7 +243,7 @@ def accept_rows(logits, gate: str = "prob"):
     logits: [..., V] float64 (finite).  m = max_v l_v; token = the smallest v
     with l_v = m.  With gate "prob" the confidence is the top-1 probability
     1 / sum_v exp(l_v - m) = softmax(l)[token] at temperature 1 ([blog]
-    "Inference").  With gate "margin" it is how far ahead the top token is,
+    "Inference").  With gate "margin" it is the top token's lead over the rest,
     read as p1 - p2: softmax(l)[token] minus the largest softmax(l)[v] over the
     other v (0 when two tokens tie at the max; p1 when V == 1).
     """

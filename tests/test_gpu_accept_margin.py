@@ -1,5 +1,5 @@
 """mars_accept_margin on the GPU against the fp64 oracle: the margin gate
-conf = p1 - p2 ([blog] "Inference": how far ahead the top token is), computed
+conf = p1 - p2 ([blog] "Inference": the top token's lead over the rest), computed
 in the same single pass over the logits, with the same commit rule and append."""
 import numpy as np
 import pytest

@@ -10,9 +10,11 @@ from ._lib import (  # noqa: F401
     MARS_DEV_TIMEOUT,
     MarsError,
     accept,
+    accept_deferred,
     accept_workspace,
     accept_workspace_size,
     decode_attn,
+    decode_attn_deferred,
     lib,
     status_string,
     train_attn,

@@ -26,6 +26,7 @@ MARS_ERR_SCRATCH_LIMIT = 5
 
 MARS_ACCEPT_MARGIN = 1
 MARS_ACCEPT_BATCH_MIN = 2
+MARS_ACCEPT_DEFERRED = 4
 
 MARS_DEV_CAPACITY = 1
 MARS_DEV_LEN_RANGE = 2
@@ -42,6 +43,7 @@ _SIGNATURES = {
     "mars_last_cuda_error": (ctypes.c_char_p, []),
     "mars_train_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "mars_decode_attn_deferred": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
     "mars_accept": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_margin": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -183,6 +185,40 @@ def decode_attn(q, k_new, v_new, k_cache, v_cache, cache_len, max_len: int, scal
     return o
 
 
+def decode_attn_deferred(q, k_new, v_new, k_cache, v_cache, cache_len, pending, max_len: int,
+                         scale: float | None = None, o=None, status=None, stream=None):
+    """Decode step of the deferred-KV sampler (include/mars.h: mars_decode_attn_deferred).
+
+    q [b, 2B, Hq, D], k_new / v_new [b, 2B, Hkv, D]: slots 0..B-1 are the previous
+    step's committed tokens (valid below pending[b]), slots B..2B-1 the new
+    placeholders.  The valid pending K/V rows are written into k_cache / v_cache
+    at cache_len; cache_len is not changed here.  Returns o [b, 2B, Hq, D]."""
+    nb, s2, hq, d = q.shape
+    if s2 % 2:
+        raise ValueError(f"q must carry 2B slots, got {s2}")
+    hkv = k_new.shape[2]
+    cap = k_cache.shape[2]
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (nb, s2, hq, d))
+    _check(k_new, "k_new", torch.bfloat16, (nb, s2, hkv, d), dev)
+    _check(v_new, "v_new", torch.bfloat16, (nb, s2, hkv, d), dev)
+    _check(k_cache, "k_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(cache_len, "cache_len", torch.int32, (nb,), dev)
+    _check(pending, "pending", torch.int32, (nb,), dev)
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, "o", torch.bfloat16, q.shape, dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_decode_attn_deferred", _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+          _ptr(cache_len), _ptr(pending), nb, s2 // 2, hq, hkv, d, cap, int(max_len), float(scale), _ptr(o),
+          _ptr(status), _stream(stream))
+    return o
+
+
 def accept_workspace_size(batch: int, B: int, V: int) -> int:
     return int(_fn("mars_accept_workspace_size")(batch, B, V))
 
@@ -229,6 +265,38 @@ def accept(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len, worksp
     _call("mars_accept_ex", _ptr(logits), nb, bq, V, float(tau), flags, _ptr(k_new), _ptr(v_new), _ptr(k_cache),
           _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
           _ptr(workspace), workspace.numel(), _stream(stream))
+    return tokens, conf, n_commit
+
+
+def accept_deferred(logits, tau: float, cache_len, n_commit, cap: int, workspace=None, tokens=None, conf=None,
+                    status=None, stream=None, gate: str = "prob", batch_min: bool = False):
+    """Acceptance step of the deferred-KV sampler (include/mars.h: mars_accept_ex
+    with MARS_ACCEPT_DEFERRED).  n_commit holds the previous step's count on
+    entry (the rows the deferred decode step just wrote): cache_len advances by
+    it, and n_commit is overwritten with this step's count.  No K/V is copied.
+    Returns (tokens, conf, n_commit)."""
+    if gate not in ("prob", "margin"):
+        raise ValueError(f"gate must be 'prob' or 'margin', got {gate!r}")
+    nb, bq, V = logits.shape
+    dev = logits.device
+    _check(logits, "logits", torch.bfloat16, (nb, bq, V))
+    _check(cache_len, "cache_len", torch.int32, (nb,), dev)
+    _check(n_commit, "n_commit", torch.int32, (nb,), dev)
+    if workspace is None:
+        workspace = accept_workspace(nb, bq, V, dev)
+    if tokens is None:
+        tokens = torch.empty((nb, bq), dtype=torch.int32, device=dev)
+    if conf is None:
+        conf = torch.empty((nb, bq), dtype=torch.float32, device=dev)
+    _check(tokens, "tokens", torch.int32, (nb, bq), dev)
+    _check(conf, "conf", torch.float32, (nb, bq), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    flags = (MARS_ACCEPT_DEFERRED | (MARS_ACCEPT_MARGIN if gate == "margin" else 0)
+             | (MARS_ACCEPT_BATCH_MIN if batch_min else 0))
+    _call("mars_accept_ex", _ptr(logits), nb, bq, V, float(tau), flags, None, None, None, None, _ptr(cache_len),
+          0, 0, int(cap), _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status), _ptr(workspace),
+          workspace.numel(), _stream(stream))
     return tokens, conf, n_commit
 
 

@@ -152,6 +152,7 @@ struct AcceptArgs {
   int32_t* status;
   int margin;           // 1: conf = p1 - p2 (margin gate); 0: conf = p1
   int batch_min;        // 1: every sequence commits the batch minimum of the counts
+  int deferred;         // 1: deferred-KV sampler: the cursor advances by the previous count, no K/V copy
   Partial* partials;    // [rows][chunks]
   int32_t* counts;      // [batch] per-sequence counts (batch-minimum mode), after the partials
   int chunks;           // chunks per row
@@ -192,8 +193,11 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vec_per_row = a.D >> 3;
   const int per_pos = a.Hkv * vec_per_row;
-  const int cand = a.B * per_pos;  // candidate 16-byte vectors of K (and of V)
+  const int cand = a.deferred ? 0 : a.B * per_pos;  // candidate 16-byte vectors of K (and of V)
   const int len0 = __ldg(a.cache_len + b);
+  // deferred-KV mode: the rows committed by the previous step, which this step's
+  // decode attention has just written at the cursor
+  const int pend = a.deferred ? a.n_commit[b] : 0;
   uint4 kpre[kPrefetch], vpre[kPrefetch];
 #pragma unroll
   for (int u = 0; u < kPrefetch; ++u) {
@@ -232,13 +236,15 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
     }
     if (lane == 0) {
       int n = max(min(__ffs(~ok) - 1, a.B), 1);
-      if (len0 < 0 || len0 + n > a.cap) {
+      const int base = len0 + pend;  // the cursor once the pending rows count
+      const bool bad = len0 < 0 || pend < 0 || pend > a.B || base > a.cap;
+      if (bad || base + n > a.cap) {
         set_status(a.status, MARS_DEV_CAPACITY);
         n = 0;
       }
-      s_n = n;
+      s_n = a.deferred ? 0 : n;
       a.n_commit[b] = n;
-      a.cache_len[b] = len0 + n;
+      a.cache_len[b] = bad ? len0 : base + (a.deferred ? 0 : n);
     }
   }
   if (a.batch_min) return;
@@ -401,6 +407,7 @@ __global__ void __launch_bounds__(256) accept_batchmin_kernel(const AcceptArgs a
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int len0 = __ldg(a.cache_len + b);
+  const int pend = a.deferred ? a.n_commit[b] : 0;  // deferred-KV mode: the previous step's count
   griddep_wait();  // the per-sequence counts are complete and visible from here on
   int m = a.B;
   for (int t = threadIdx.x; t < a.batch; t += blockDim.x) m = min(m, __ldcg(a.counts + t));
@@ -410,17 +417,21 @@ __global__ void __launch_bounds__(256) accept_batchmin_kernel(const AcceptArgs a
   __syncthreads();
   int n = s_min[0];
   for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) n = min(n, s_min[w]);
-  if (len0 < 0 || len0 + n > a.cap) {
+  const int base = len0 + pend;
+  const bool bad = len0 < 0 || pend < 0 || pend > a.B || base > a.cap;
+  if (bad || base + n > a.cap) {
     if (threadIdx.x == 0) {
       set_status(a.status, MARS_DEV_CAPACITY);
       a.n_commit[b] = 0;
+      if (!bad) a.cache_len[b] = base;
     }
     return;
   }
   if (threadIdx.x == 0) {
     a.n_commit[b] = n;
-    a.cache_len[b] = len0 + n;
+    a.cache_len[b] = base + (a.deferred ? 0 : n);
   }
+  if (a.deferred) return;
   const int vec_per_row = a.D >> 3;
   const int per_pos = a.Hkv * vec_per_row;
   for (int e = threadIdx.x; e < n * per_pos; e += blockDim.x) {
@@ -494,16 +505,18 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
 int check_args(const uint16_t* logits, int batch, int B, int V, float tau, const uint16_t* k_new,
                const uint16_t* v_new, const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* cache_len,
                int Hkv, int D, int cap, const int32_t* tokens, const float* conf, const int32_t* n_commit,
-               const int32_t* status) {
+               const int32_t* status, bool with_kv = true) {
   using mars_host::aligned16;
   using mars_host::aligned2;
   using mars_host::aligned4;
-  MARS_HOST_CHECK(batch > 0 && B > 0 && B <= 16 && V > 0 && Hkv > 0 && D > 0 && D % 8 == 0 && D <= 256 && cap > 0,
-                  MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(batch > 0 && B > 0 && B <= 16 && V > 0 && cap > 0, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(static_cast<long long>(batch) * B * chunks_for(V) < (1LL << 31), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(!isnan(tau), MARS_ERR_INVALID_ARG);
-  const void* vec16[] = {k_new, v_new, k_cache, v_cache};
-  for (const void* p : vec16) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  if (with_kv) {
+    MARS_HOST_CHECK(Hkv > 0 && D > 0 && D % 8 == 0 && D <= 256, MARS_ERR_INVALID_ARG);
+    const void* vec16[] = {k_new, v_new, k_cache, v_cache};
+    for (const void* p : vec16) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  }
   const void* word4[] = {cache_len, tokens, conf, n_commit};
   for (const void* p : word4) MARS_HOST_CHECK(p != nullptr && aligned4(p), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(logits != nullptr && aligned2(logits), MARS_ERR_INVALID_ARG);
@@ -534,6 +547,7 @@ AcceptArgs make_args(const uint16_t* logits, int batch, int B, int V, float tau,
   a.status = status;
   a.margin = 0;
   a.batch_min = 0;
+  a.deferred = 0;
   a.partials = nullptr;
   a.counts = nullptr;
   a.chunks = a.items = 0;
@@ -552,10 +566,12 @@ extern "C" int mars_accept_ex(const uint16_t* logits, int batch, int B, int V, f
                               int32_t* cache_len, int Hkv, int D, int cap, int32_t* tokens, float* conf,
                               int32_t* n_commit, int32_t* status, void* workspace, size_t workspace_bytes,
                               void* stream) {
+  MARS_HOST_CHECK((flags & ~(MARS_ACCEPT_MARGIN | MARS_ACCEPT_BATCH_MIN | MARS_ACCEPT_DEFERRED)) == 0,
+                  MARS_ERR_INVALID_ARG);
+  const bool deferred = (flags & MARS_ACCEPT_DEFERRED) != 0;
   int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
-                      conf, n_commit, status);
+                      conf, n_commit, status, !deferred);
   if (rc != MARS_OK) return rc;
-  MARS_HOST_CHECK((flags & ~(MARS_ACCEPT_MARGIN | MARS_ACCEPT_BATCH_MIN)) == 0, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(workspace != nullptr && mars_host::aligned16(workspace), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(workspace_bytes >= ws_bytes(batch, B, V), MARS_ERR_WORKSPACE_TOO_SMALL);
   rc = mars_host::check_device();
@@ -565,6 +581,7 @@ extern "C" int mars_accept_ex(const uint16_t* logits, int batch, int B, int V, f
                            conf, n_commit, status);
   a.margin = (flags & MARS_ACCEPT_MARGIN) ? 1 : 0;
   a.batch_min = (flags & MARS_ACCEPT_BATCH_MIN) ? 1 : 0;
+  a.deferred = deferred ? 1 : 0;
   a.partials = static_cast<Partial*>(workspace);
   a.counts = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + partial_bytes(batch, B, V));
   return launch(a, static_cast<cudaStream_t>(stream));

@@ -31,6 +31,15 @@
 //     whatever the cache holds there (even NaN) never reaches the output.
 //   * Units are visited longest-cache-first (a rank computed in every CTA from
 //     cache_len), so the long sequences start early and short ones fill in.
+//   * Deferred-KV mode (the blog post's deferred-KV sampler: KV commitment
+//     deferred into the next proposal forward, per-sample cursors, a
+//     cache-validity bitmask).  A sequence carries S = 2B slots: slots 0..B-1
+//     are the tokens committed by the previous step (valid below pending[b]),
+//     slots B..2B-1 the new placeholders.  A slot's validity bit masks it as a
+//     key and, as a query, makes its output row zero; V rows of invalid slots
+//     are zeroed in shared memory.  The CTA that loads the new tile of head
+//     chunk 0 also writes the valid pending K/V rows into the cache at the
+//     cursor, so no separate forward or cache copy commits them.
 // Every mbarrier wait is bounded; a wait that gives up sets MARS_DEV_TIMEOUT.
 #include <cuda.h>
 
@@ -74,9 +83,15 @@ struct DCfg {
 
 struct DecodeArgs {
   const int32_t* cache_len;
+  const int32_t* pending;  // deferred-KV mode: valid pending slots per sequence; nullptr otherwise
+  const uint16_t* k_new;   // [batch, S, Hkv, D] (read by the fused append of pending rows)
+  const uint16_t* v_new;
+  uint16_t* k_cache;       // [batch, Hkv, cap, D] (written by the fused append)
+  uint16_t* v_cache;
   uint16_t* o;
   int32_t* status;
   int batch, B, Hq, Hkv, cap, max_len;
+  int S;             // query / new-key slots per sequence: B, or 2B in deferred-KV mode
   float scale_log2;  // scale * log2(e)
   int G;             // Hq / Hkv
   int Gc;            // query heads per unit
@@ -120,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit_rank = blockIdx.x / a.C;
   const int crank = static_cast<int>(cluster_ctarank());
 
-  const int R = a.Gc * a.B;            // rows loaded (row = i * Gc + head)
+  const int R = a.Gc * a.S;            // rows loaded (row = slot i * Gc + head)
   const int act_warps = (R + 31) / 32;  // softmax warps per stream with real rows
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -166,19 +181,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int heads = min(a.Gc, a.G - hc * a.Gc);  // real heads in this unit
 
   const int len = a.sort_units ? s_len[b] : __ldg(a.cache_len + b);
-  if (len < 0 || len > a.max_len) {
+  const bool deferred = a.pending != nullptr;
+  const int pend = deferred ? __ldg(a.pending + b) : 0;
+  const bool len_bad = len < 0 || len > a.max_len || pend < 0 || pend > a.B;
+  if (len_bad || len + pend > a.cap) {
     // Uniform over the cluster: every CTA of the unit sees the same len and returns here.
     if (crank == 0) {
-      if (tid == 0) set_status(a.status, MARS_DEV_LEN_RANGE);
-      for (int e = tid; e < heads * a.B * (D / 8); e += kThreads) {
+      if (tid == 0) set_status(a.status, len_bad ? MARS_DEV_LEN_RANGE : MARS_DEV_CAPACITY);
+      for (int e = tid; e < heads * a.S * (D / 8); e += kThreads) {
         const int r = e / (D / 8), c = e % (D / 8);
-        const int hl = r / a.B, i = r % a.B;
-        *reinterpret_cast<uint4*>(a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 8 * c) =
+        const int hl = r / a.S, i = r % a.S;
+        *reinterpret_cast<uint4*>(a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 8 * c) =
             make_uint4(0, 0, 0, 0);
       }
     }
     return;
   }
+  // slot validity bitmask: every slot, or (deferred) the pending slots below pend and all placeholders
+  const uint32_t vmask = deferred ? ((1u << pend) - 1u) | (((1u << a.B) - 1u) << a.B) : (1u << a.S) - 1u;
   const int nct = (len + kTileKeys - 1) / kTileKeys;  // cache tiles of the unit
   const int t0 = static_cast<int>((static_cast<long long>(nct) * crank) / a.C);
   const int t1 = static_cast<int>((static_cast<long long>(nct) * (crank + 1)) / a.C);
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < C::NB; ++c) tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
     for (int k = 0; k < min(ncache, C::NS); ++k) load_tile(k);
     if (has_new) {
-      mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.B);
+      mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.S);
       for (int c = 0; c < C::NB; ++c) {
         tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, b);
         tma_load_4d(nv_s + c * C::N_BOX, &tm_vn, &bar_new, 64 * c, g, 0, b);
@@ -217,13 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- zero the rows the TMA loads never write (Q rows >= R, new-key rows >= B):
+  // ---- zero the rows the TMA loads never write (Q rows >= R, new-key rows >= S):
   // the tail of every Q box and of every new-key box
   for (int bx = 0; bx < C::NB; ++bx)
     for (int e = tid; e < (kRows - R) * 8; e += kThreads) st_shared_v4(q_s + bx * C::Q_BOX + R * 128 + e * 16, 0u, 0u, 0u, 0u);
   for (int bx = 0; bx < 2 * C::NB; ++bx)  // new K boxes, then new V boxes
-    for (int e = tid; e < (kNewKeys - a.B) * 8; e += kThreads)
-      st_shared_v4(nk_s + bx * C::N_BOX + a.B * 128 + e * 16, 0u, 0u, 0u, 0u);
+    for (int e = tid; e < (kNewKeys - a.S) * 8; e += kThreads)
+      st_shared_v4(nk_s + bx * C::N_BOX + a.S * 128 + e * 16, 0u, 0u, 0u, 0u);
   fence_async_smem();
   if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -245,6 +265,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    if (deferred && has_new && hc == 0) {
+      // Commit the valid pending rows of KV head g at the cursor.  Other CTAs of
+      // this sequence may load these cache rows inside their last tile at the same
+      // time; they mask them (keys at or past cache_len), so either value is fine.
+      constexpr int vpr = D / 8;  // 16-byte vectors per row
+      for (int e = lane; e < pend * vpr; e += 32) {
+        const int i = e / vpr, c = e % vpr;
+        const size_t src = ((static_cast<size_t>(b) * a.S + i) * a.Hkv + g) * D + 8 * c;
+        const size_t dst = ((static_cast<size_t>(b) * a.Hkv + g) * a.cap + len + i) * D + 8 * c;
+        *reinterpret_cast<uint4*>(a.k_cache + dst) = *reinterpret_cast<const uint4*>(a.k_new + src);
+        *reinterpret_cast<uint4*>(a.v_cache + dst) = *reinterpret_cast<const uint4*>(a.v_new + src);
+      }
+    }
   } else if (warp == 1) {
     // ================= MMA issuer.  The whole warp runs the schedule, so the
     // descriptors stay warp-uniform; one elected lane issues the tcgen05
@@ -330,7 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_col = tmem + lane_addr + x * kTileKeys;
     const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
-    const int pos = r / a.Gc;  // query position i of this row (rows >= R are padding)
+    const int slot = r / a.Gc;  // query slot i of this row (rows >= R are padding)
+    // A valid query slot sees the valid new keys up to itself; padding rows and
+    // invalid slots see nothing (their outputs are zero or never written).
+    const bool row_valid = slot < a.S && ((vmask >> slot) & 1u);
+    const uint32_t new_vis = row_valid ? vmask & ((2u << slot) - 1u) : 0u;
     float m_used = -INFINITY, l = 0.f;
     int nmine = 0;
     if (active) {
@@ -341,14 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // last visible column of this tile for this row
         const bool is_new = k >= ncache;
         const int key0 = (t0 + k) * kTileKeys;
-        const int vlast = is_new ? pos : len - 1 - key0;
+        const int vlast = row_valid ? len - 1 - key0 : -1;
         uint32_t s[kTileKeys];
         tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tc_wait_ld();
-        if (is_new || vlast < kTileKeys - 1) {
+        if (is_new) {
 #pragma unroll
-          for (int c = 0; c < kTileKeys; ++c) s[c] = c <= vlast ? s[c] : 0xFF800000u;  // -inf
+          for (int c = 0; c < kTileKeys; ++c)
+            s[c] = (c < kNewKeys && ((new_vis >> c) & 1u)) ? s[c] : 0xFF800000u;  // -inf
+        } else if (vlast < kTileKeys - 1) {
+#pragma unroll
+          for (int c = 0; c < kTileKeys; ++c) s[c] = c <= vlast ? s[c] : 0xFF800000u;
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -391,6 +432,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(s_col + (c >> 1), pw);
         }
         l = l * alpha + (sum0 + sum1);
+        // Invalid pending slots of the new tile may hold anything (even NaN): zero
+        // their V rows so that P = 0 meets finite values.
+        if (is_new && deferred && pend < a.B) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_new, 0));
+          if (!ok) break;
+          const int per_box = (a.B - pend) * 8;  // 16-byte chunks of rows pend .. B-1
+          for (int e = quad * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
+            const int bx = e / per_box, w = e % per_box;
+            st_shared_v4(nv_s + bx * C::N_BOX + pend * 128 + w * 16, 0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        }
         // The last cache tile can hold keys at or past cache_len: zero those V rows
         // (whole 128-byte rows of every box) so that P = 0 meets finite values.
         if (!is_new && len - key0 < kTileKeys) {
@@ -474,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lsum += m[q] * l[q];
         }
       }
-      const float inv = 1.f / lsum;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
 #pragma unroll
       for (int q = 0; q < 2 * kMaxCluster; ++q)
         if (q < ns) w_s[(r - r_lo) * 2 * kMaxCluster + q] = m[q] * inv;
@@ -501,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.w += w[q] * v[q].w;
         }
       }
-      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.B + i) * a.Hq + h0 + hl) * D + 4 * d4;
+      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
       *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
     }
   }
@@ -584,30 +637,38 @@ inline int pow2_ceil(int x) {
   return p;
 }
 
-}  // namespace
-
-extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
-                                const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* cache_len, int batch,
-                                int B, int Hq, int Hkv, int D, int cap, int max_len, float scale, uint16_t* o,
-                                int32_t* status, void* stream) {
+// Shared host path of both entry points: pending == nullptr is the plain step
+// (S = B slots), otherwise the deferred-KV step (S = 2B slots).
+int decode_impl(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, const uint16_t* k_cache,
+                const uint16_t* v_cache, uint16_t* k_cache_w, uint16_t* v_cache_w, const int32_t* cache_len,
+                const int32_t* pending, int batch, int B, int Hq, int Hkv, int D, int cap, int max_len, float scale,
+                uint16_t* o, int32_t* status, cudaStream_t stream) {
   using mars_host::aligned16;
-  MARS_HOST_CHECK(batch > 0 && B >= 1 && B <= 16 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0, MARS_ERR_INVALID_ARG);
+  const int S = pending != nullptr ? 2 * B : B;
+  MARS_HOST_CHECK(batch > 0 && B >= 1 && S <= kNewKeys && Hq > 0 && Hkv > 0 && Hq % Hkv == 0, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(D == 64 || D == 128, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(cap > 0 && max_len >= 0 && max_len <= cap, MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(scale > 0.f && scale < INFINITY, MARS_ERR_INVALID_ARG);
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* p : ptrs) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(cache_len != nullptr && mars_host::aligned4(cache_len), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(pending == nullptr || mars_host::aligned4(pending), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(status == nullptr || mars_host::aligned4(status), MARS_ERR_INVALID_ARG);
   int rc = mars_host::check_device();
   if (rc != MARS_OK) return rc;
 
   DecodeArgs a;
   a.cache_len = cache_len;
+  a.pending = pending;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache_w;
+  a.v_cache = v_cache_w;
   a.o = o;
   a.status = status;
   a.batch = batch;
   a.B = B;
+  a.S = S;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.cap = cap;
@@ -615,7 +676,7 @@ extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const 
   a.scale_log2 = scale * kLog2e;
   a.G = Hq / Hkv;
   // Heads per unit: as many as fit in the 128 rows of one MMA tile.
-  a.Gc = std::min(a.G, kRows / B);
+  a.Gc = std::min(a.G, kRows / S);
   a.nhc = ceil_div(a.G, a.Gc);
   const long long units = static_cast<long long>(batch) * Hkv * a.nhc;
   MARS_HOST_CHECK(units * kMaxCluster < (1LL << 31), MARS_ERR_INVALID_ARG);
@@ -631,11 +692,30 @@ extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const 
   a.box_rows = std::min(cap, kTileKeys);
 
   Maps mp;
-  const long long dq[4] = {D, Hq, B, batch}, dc[4] = {D, cap, Hkv, batch}, dn[4] = {D, Hkv, B, batch};
-  if (!make_map(&mp.q, q, dq, a.Gc, B) || !make_map(&mp.kc, k_cache, dc, a.box_rows, 1) ||
-      !make_map(&mp.vc, v_cache, dc, a.box_rows, 1) || !make_map(&mp.kn, k_new, dn, 1, B) ||
-      !make_map(&mp.vn, v_new, dn, 1, B))
+  const long long dq[4] = {D, Hq, S, batch}, dc[4] = {D, cap, Hkv, batch}, dn[4] = {D, Hkv, S, batch};
+  if (!make_map(&mp.q, q, dq, a.Gc, S) || !make_map(&mp.kc, k_cache, dc, a.box_rows, 1) ||
+      !make_map(&mp.vc, v_cache, dc, a.box_rows, 1) || !make_map(&mp.kn, k_new, dn, 1, S) ||
+      !make_map(&mp.vn, v_new, dn, 1, S))
     return MARS_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return D == 64 ? launch<64>(mp, a, static_cast<int>(units), s) : launch<128>(mp, a, static_cast<int>(units), s);
+  return D == 64 ? launch<64>(mp, a, static_cast<int>(units), stream)
+                 : launch<128>(mp, a, static_cast<int>(units), stream);
+}
+
+}  // namespace
+
+extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* cache_len, int batch,
+                                int B, int Hq, int Hkv, int D, int cap, int max_len, float scale, uint16_t* o,
+                                int32_t* status, void* stream) {
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, nullptr, nullptr, cache_len, nullptr, batch, B, Hq, Hkv, D,
+                     cap, max_len, scale, o, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mars_decode_attn_deferred(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                         uint16_t* k_cache, uint16_t* v_cache, const int32_t* cache_len,
+                                         const int32_t* pending, int batch, int B, int Hq, int Hkv, int D, int cap,
+                                         int max_len, float scale, uint16_t* o, int32_t* status, void* stream) {
+  MARS_HOST_CHECK(pending != nullptr, MARS_ERR_INVALID_ARG);
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, k_cache, v_cache, cache_len, pending, batch, B, Hq, Hkv, D,
+                     cap, max_len, scale, o, status, static_cast<cudaStream_t>(stream));
 }

@@ -207,7 +207,7 @@ def step_logits(shape: DecodeShape, step: int, seed_key=0, spike_lo=None, spike_
     hi = shape.spike_hi if spike_hi is None else spike_hi
     exact = None
     if shape is TINY_DECODE:
-        # "a random 50% of positions": exactly half of the B positions.
+        # half of the positions, chosen at random: exactly B / 2 of them.
         exact = shape.B // 2
     return spiked_logits(shape.batch, shape.B, shape.V, shape.base_sigma, shape.spike_prob,
                          lo, hi, g, exact_spike_count=exact)
