@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_q, bar_new, bar_kv[C::NS], bar_kv_empty[C::NS], bar_s[2], bar_p[2], bar_o[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_b;
+  __shared__ float s_mstate[2][kRows], s_lstate[2][kRows];  // single-CTA units: each stream's (m, l) per row
   __shared__ int s_len[kSortLimit];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -466,31 +467,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && nmine > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[x], 0));
       if (!ok && lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
     }
-    // Both streams' products are complete once every softmax warp is past its
-    // wait above, so the ring (every loaded tile consumed) can hold the merge state.
-    named_bar_sync(1, 256);
-    tc_fence_after();
-    float* acc_s = reinterpret_cast<float*>(smem + C::RING_OFF);  // [2][128][D], 16-byte units XOR (row & 7)
-    float* m_s = acc_s + 2 * kRows * D;                           // [2][128]
-    float* l_s = m_s + 2 * kRows;                                 // [2][128]
-    if (active) {
-      float4* dst = reinterpret_cast<float4*>(acc_s + (x * kRows + r) * D);
-      const bool have = ok && nmine > 0;
+    const bool have = ok && nmine > 0;
+    if (a.C == 1) {
+      // ---- one CTA per unit: combine the two streams of each row straight from
+      // tensor memory.  Thread (stream x, row r) writes columns [x D/2, (x+1) D/2)
+      // of the row, reading both streams' O there.
+      if (active) {
+        s_mstate[x][r] = have ? m_used : -INFINITY;
+        s_lstate[x][r] = have ? l : 0.f;
+      }
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      if (active) {
+        const float m0 = s_mstate[0][r], m1 = s_mstate[1][r];
+        const float mmax = fmaxf(m0, m1);
+        float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mmax);
+        float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mmax);
+        const float lsum = w0 * s_lstate[0][r] + w1 * s_lstate[1][r];
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: a row that sees no key (padding, invalid slot)
+        w0 *= inv;
+        w1 *= inv;
+        const int i = r / a.Gc, hl = r % a.Gc;
+        const bool store = r < R && hl < heads;
+        const uint32_t oa = tmem + lane_addr + C::O_COL + x * (D / 2);  // stream A's O, this half
+        const uint32_t ob = oa + D;                                      // stream B's O, this half
+        uint4* dst = reinterpret_cast<uint4*>(a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D +
+                                              x * (D / 2));
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32(o_col + c, ov);
-        tc_wait_ld();
+        for (int c = 0; c < D / 2; c += 32) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(oa + c, va);
+          tmem_ld32(ob + c, vb);
+          tc_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                              __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-          dst[((c >> 2) + e) ^ (r & 7)] = v;
+          for (int e = 0; e < 16; ++e) {
+            // a stream without tiles never wrote its O: its weight is 0 and its columns are not read
+            const float f0 = (w0 != 0.f ? w0 * __uint_as_float(va[2 * e]) : 0.f) +
+                             (w1 != 0.f ? w1 * __uint_as_float(vb[2 * e]) : 0.f);
+            const float f1 = (w0 != 0.f ? w0 * __uint_as_float(va[2 * e + 1]) : 0.f) +
+                             (w1 != 0.f ? w1 * __uint_as_float(vb[2 * e + 1]) : 0.f);
+            pk[e] = pack_bf16x2(f0, f1);
+          }
+          if (store) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[(c >> 3) + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
         }
       }
-      m_s[x * kRows + r] = have ? m_used : -INFINITY;
-      l_s[x * kRows + r] = have ? l : 0.f;
+    } else {
+      // Both streams' products are complete once every softmax warp is past its
+      // wait above, so the ring (every loaded tile consumed) can hold the merge state.
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      float* acc_s = reinterpret_cast<float*>(smem + C::RING_OFF);  // [2][128][D], 16-byte units XOR (row & 7)
+      float* m_s = acc_s + 2 * kRows * D;                           // [2][128]
+      float* l_s = m_s + 2 * kRows;                                 // [2][128]
+      if (active) {
+        float4* dst = reinterpret_cast<float4*>(acc_s + (x * kRows + r) * D);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(o_col + c, ov);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                                __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[((c >> 2) + e) ^ (r & 7)] = v;
+          }
+        }
+        m_s[x * kRows + r] = have ? m_used : -INFINITY;
+        l_s[x * kRows + r] = have ? l : 0.f;
+      }
     }
   }
 
@@ -498,67 +549,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This CTA finishes rows [r_lo, r_hi): first one weight per (row, state),
   // w = 2^(m - max m) / sum_states(2^(m - max m) l), then O = sum w acc.
   tc_fence_before();
-  cluster_sync();
-  {
-    const float* acc_s = reinterpret_cast<const float*>(smem + C::RING_OFF);
-    const float* m_s = acc_s + 2 * kRows * D;
-    const float* l_s = m_s + 2 * kRows;
-    float* w_s = const_cast<float*>(l_s) + 2 * kRows;  // [rows_per][2 * kMaxCluster], this CTA's own
-    const uint32_t acc_l = smem_u32(acc_s), m_l = smem_u32(m_s), l_l = smem_u32(l_s);
-    const int rows_per = (R + a.C - 1) / a.C;
-    const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
-    const int ns = 2 * a.C;  // states per row
-    for (int r = r_lo + tid; r < r_hi; r += kThreads) {
-      float m[2 * kMaxCluster], l[2 * kMaxCluster];
-      float mmax = -INFINITY;
+  if (a.C > 1) {
+    cluster_sync();
+    {
+      const float* acc_s = reinterpret_cast<const float*>(smem + C::RING_OFF);
+      const float* m_s = acc_s + 2 * kRows * D;
+      const float* l_s = m_s + 2 * kRows;
+      float* w_s = const_cast<float*>(l_s) + 2 * kRows;  // [rows_per][2 * kMaxCluster], this CTA's own
+      const uint32_t acc_l = smem_u32(acc_s), m_l = smem_u32(m_s), l_l = smem_u32(l_s);
+      const int rows_per = (R + a.C - 1) / a.C;
+      const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
+      const int ns = 2 * a.C;  // states per row
+      for (int r = r_lo + tid; r < r_hi; r += kThreads) {
+        float m[2 * kMaxCluster], l[2 * kMaxCluster];
+        float mmax = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 2 * kMaxCluster; ++q) {
-        if (q < ns) {
-          m[q] = dsmem_ld_f32(dsmem_map(m_l + 4 * ((q & 1) * kRows + r), q >> 1));
-          l[q] = dsmem_ld_f32(dsmem_map(l_l + 4 * ((q & 1) * kRows + r), q >> 1));
-          mmax = fmaxf(mmax, m[q]);
+        for (int q = 0; q < 2 * kMaxCluster; ++q) {
+          if (q < ns) {
+            m[q] = dsmem_ld_f32(dsmem_map(m_l + 4 * ((q & 1) * kRows + r), q >> 1));
+            l[q] = dsmem_ld_f32(dsmem_map(l_l + 4 * ((q & 1) * kRows + r), q >> 1));
+            mmax = fmaxf(mmax, m[q]);
+          }
         }
-      }
-      float lsum = 0.f;
+        float lsum = 0.f;
 #pragma unroll
-      for (int q = 0; q < 2 * kMaxCluster; ++q) {
-        if (q < ns) {
-          m[q] = m[q] == -INFINITY ? 0.f : fast_exp2(m[q] - mmax);
-          lsum += m[q] * l[q];
+        for (int q = 0; q < 2 * kMaxCluster; ++q) {
+          if (q < ns) {
+            m[q] = m[q] == -INFINITY ? 0.f : fast_exp2(m[q] - mmax);
+            lsum += m[q] * l[q];
+          }
         }
-      }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
 #pragma unroll
-      for (int q = 0; q < 2 * kMaxCluster; ++q)
-        if (q < ns) w_s[(r - r_lo) * 2 * kMaxCluster + q] = m[q] * inv;
+        for (int q = 0; q < 2 * kMaxCluster; ++q)
+          if (q < ns) w_s[(r - r_lo) * 2 * kMaxCluster + q] = m[q] * inv;
+      }
+      __syncthreads();
+      for (int e = tid; e < (r_hi - r_lo) * (D / 4); e += kThreads) {
+        const int r = r_lo + e / (D / 4);
+        const int d4 = e % (D / 4);
+        const int i = r / a.Gc, hl = r % a.Gc;
+        if (hl >= heads) continue;
+        const float* w = w_s + (r - r_lo) * 2 * kMaxCluster;
+        const uint32_t off = acc_l + 4 * (r * D + 4 * (d4 ^ (r & 7)));
+        float4 v[2 * kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < 2 * kMaxCluster; ++q)
+          if (q < ns) v[q] = dsmem_ld_f32x4(dsmem_map(off + 4 * (q & 1) * kRows * D, q >> 1));
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 2 * kMaxCluster; ++q) {
+          if (q < ns) {
+            o.x += w[q] * v[q].x;
+            o.y += w[q] * v[q].y;
+            o.z += w[q] * v[q].z;
+            o.w += w[q] * v[q].w;
+          }
+        }
+        uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+      }
     }
-    __syncthreads();
-    for (int e = tid; e < (r_hi - r_lo) * (D / 4); e += kThreads) {
-      const int r = r_lo + e / (D / 4);
-      const int d4 = e % (D / 4);
-      const int i = r / a.Gc, hl = r % a.Gc;
-      if (hl >= heads) continue;
-      const float* w = w_s + (r - r_lo) * 2 * kMaxCluster;
-      const uint32_t off = acc_l + 4 * (r * D + 4 * (d4 ^ (r & 7)));
-      float4 v[2 * kMaxCluster];
-#pragma unroll
-      for (int q = 0; q < 2 * kMaxCluster; ++q)
-        if (q < ns) v[q] = dsmem_ld_f32x4(dsmem_map(off + 4 * (q & 1) * kRows * D, q >> 1));
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < 2 * kMaxCluster; ++q) {
-        if (q < ns) {
-          o.x += w[q] * v[q].x;
-          o.y += w[q] * v[q].y;
-          o.z += w[q] * v[q].z;
-          o.w += w[q] * v[q].w;
-        }
-      }
-      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
-    }
+    cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+  } else {
+    __syncthreads();  // every tensor-memory read of the epilogue is done
   }
-  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
