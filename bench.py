@@ -442,9 +442,9 @@ def run_gpu(args, rank, world, local):
 
     # end to end through the public API with pinned host buffers
     e2e = run_e2e(args, mars, train05, device, stream, dist, world)
-    graph = None if args.no_graph else run_b1_graph(args, mars, dec1, device)
-    if graph is not None:
-        parts["decode_step_b1"]["graph_steps_per_s"] = graph
+    if not args.no_graph:
+        parts["decode_step_b1"].update(run_graph(mars, dec1, device, peaks["hbm_gbs"]))
+        parts["decode_step_b64"].update(run_graph(mars, dec64, device, peaks["hbm_gbs"]))
     # variants of the accept row, timed on their own after the step loop: the margin
     # gate and the batch-minimum cache mode (the paper's original sampler)
     parts["accept_margin_b64"] = run_accept_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic,
@@ -618,13 +618,15 @@ def run_deferred_variant(args, mars, work, device, hbm_peak, traffic, gen):
     }
 
 
-def run_b1_graph(args, mars, work, device):
-    """Batch-1 decode loop (decode attention + accept) captured as one CUDA graph of 256 steps."""
+def run_graph(mars, work, device, hbm_peak):
+    """A whole decode episode (decode attention + accept per step: 256 steps at batch 1,
+    128 at batch 64) captured as one CUDA graph; device-side steps/s and the
+    algorithmic GB/s of the episode."""
     import torch
 
     n_steps = work.s.steps
     stream = torch.cuda.Stream(device=device)
-    n_out = torch.zeros((n_steps, 1), dtype=torch.int32, device=device)
+    n_out = torch.zeros((n_steps, work.s.batch), dtype=torch.int32, device=device)
     with torch.cuda.stream(stream):
         work.reset()
         for i in range(2):
@@ -650,7 +652,13 @@ def run_b1_graph(args, mars, work, device):
             e1.record(stream)
             stream.synchronize()
             ms += e0.elapsed_time(e1)
-    return round(reps * n_steps / (ms * 1e-3), 1)
+    hist = n_out.cpu().numpy()
+    records = [("reset", 0, None)] + [("step", i % work.nsets, hist[i]) for i in range(n_steps)]
+    dec_b, acc_b = work.byte_counts(records)
+    work.reset()
+    gbs = reps * (sum(dec_b) + sum(acc_b)) / (ms * 1e-3) / 1e9
+    return {"graph_steps_per_s": round(reps * n_steps / (ms * 1e-3), 1), "graph_GB_per_s": round(gbs, 1),
+            "graph_frac_of_hbm": round(gbs / hbm_peak, 4)}
 
 
 # --------------------------------------------------------------------------
@@ -787,7 +795,7 @@ def main():
     p.add_argument("--impl", choices=["mars", "reference"], default="mars")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph batch-1 decode loop")
+    p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph decode episodes (batch 1 and 64)")
     p.add_argument("--profile", choices=["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1",
                                          "accept_b1", "accept_margin_b64", "decode_attn_deferred_b64",
                                          "accept_deferred_b64"],

@@ -158,16 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.sort_units) {
     for (int t = tid; t < a.batch; t += kThreads) s_len[t] = __ldg(a.cache_len + t);
     __syncthreads();
-    // rank(t) = #{u : len_u > len_t, or len_u == len_t and u < t}, 32 u at a time per warp
-    for (int t = warp; t < a.batch; t += kThreads / 32) {
+    // rank(t) = #{u : len_u > len_t, or len_u == len_t and u < t}: one thread per t,
+    // every thread of a warp reading the same s_len[u] (a broadcast)
+    for (int t = tid; t < a.batch; t += kThreads) {
       const int lt = s_len[t];
       int rank = 0;
-      for (int u0 = 0; u0 < a.batch; u0 += 32) {
-        const int u = u0 + lane;
-        const int lu = u < a.batch ? s_len[u] : -1;
-        rank += __popc(__ballot_sync(0xffffffffu, u < a.batch && (lu > lt || (lu == lt && u < t))));
+      for (int u = 0; u < a.batch; ++u) {
+        const int lu = s_len[u];
+        rank += (lu > lt || (lu == lt && u < t)) ? 1 : 0;
       }
-      if (lane == 0 && rank == b_rank) s_b = t;
+      if (rank == b_rank) s_b = t;
     }
     __syncthreads();
   } else {
