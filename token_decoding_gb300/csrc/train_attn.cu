@@ -417,40 +417,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // visible columns of this row inside the tile: [vlo, vhi] (empty when vlo > vhi)
         const int vlo = part ? max((nz ? n_lo_v : 0) - kstart, 0) : 0;
         const int vhi = part ? min((nz ? n_hi_v : c_hi_v) - kstart, kBN - 1) : kBN - 1;
-        // D = 64: one pass, all of S in registers (the softmax is the bottleneck here).
-        // D = 128: two passes over S in TMEM, 64 columns at a time (half the registers):
-        // the row max, then exp2 and the bf16 store of P.  Hidden scores become -inf
-        // (exp2 of them is exactly 0).
-        constexpr int SPAN = D == 64 ? kBN : 64;  // columns held in registers at a time
-        auto load_span = [&](int h, uint32_t (&v)[SPAN]) {
+        // One pass: the row's 128 scores are read from tensor memory once and kept in
+        // registers for the max and then exp2 and the bf16 store of P.  Hidden scores
+        // become -inf (exp2 of them is exactly 0).
+        uint32_t v0[kBN];
 #pragma unroll
-          for (int c = 0; c < SPAN; c += 32) tmem_ld32(s_col + SPAN * h + c, *reinterpret_cast<uint32_t(*)[32]>(&v[c]));
-          tc_wait_ld();
-          if (part) {
+        for (int c = 0; c < kBN; c += 32) tmem_ld32(s_col + c, *reinterpret_cast<uint32_t(*)[32]>(&v0[c]));
+        tc_wait_ld();
+        if (part) {
 #pragma unroll
-            for (int c = 0; c < SPAN; ++c) v[c] = (SPAN * h + c >= vlo && SPAN * h + c <= vhi) ? v[c] : 0xFF800000u;
-          }
-        };
-        auto span_max = [&](const uint32_t (&v)[SPAN], float& m0, float& m1, float& m2, float& m3) {
-#pragma unroll
-          for (int c = 0; c < SPAN; c += 8) {
-            m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-            m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-            m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-            m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-          }
-        };
+          for (int c = 0; c < kBN; ++c) v0[c] = (c >= vlo && c <= vhi) ? v0[c] : 0xFF800000u;
+        }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-        uint32_t v0[SPAN];  // D = 64: S, kept for the exp pass
-        if constexpr (SPAN == kBN) {
-          load_span(0, v0);
-          span_max(v0, mx0, mx1, mx2, mx3);
-        } else {
-#pragma unroll 1
-          for (int h = 0; h < kBN / SPAN; ++h) {
-            load_span(h, v0);
-            span_max(v0, mx0, mx1, mx2, mx3);
-          }
+#pragma unroll
+        for (int c = 0; c < kBN; c += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(v0[c + 2]), __uint_as_float(v0[c + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(v0[c + 4]), __uint_as_float(v0[c + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(v0[c + 6]), __uint_as_float(v0[c + 7]));
         }
         const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
         // lazy rescale: keep the old reference max unless the new one is 2^8 larger.
@@ -477,39 +461,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // keys [32q, 32q + 32) -> hi in columns [16q, 16q + 16); on split tiles hi in
         // [32q, 32q + 16) and lo = P - hi in [32q + 16, 32q + 32).
         uint64_t sum2x = 0;  // two fp32 partial sums (bits of +0.0f)
-#pragma unroll 1
-        for (int h = 0; h < kBN / SPAN; ++h) {
-          if constexpr (SPAN != kBN) load_span(h, v0);
 #pragma unroll
-          for (int qq = 0; qq < SPAN / 32; ++qq) {
-            const int q = (SPAN / 32) * h + qq;
-            if (!split) {
-              uint32_t hi[16];
+        for (int q = 0; q < kBN / 32; ++q) {
+          if (!split) {
+            uint32_t hi[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                float x0, x1;
-                fma2(__uint_as_float(v0[32 * qq + 2 * e]), __uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2,
-                     neg_mu, x0, x1);
-                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                add2(sum2x, p0, p1);
-                hi[e] = pack_bf16x2(p0, p1);
-              }
-              tmem_st16(s_col + 16 * q, hi);
-            } else {
-              uint32_t hi[16], lo[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                float x0, x1;
-                fma2(__uint_as_float(v0[32 * qq + 2 * e]), __uint_as_float(v0[32 * qq + 2 * e + 1]), a.scale_log2,
-                     neg_mu, x0, x1);
-                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                add2(sum2x, p0, p1);
-                hi[e] = pack_bf16x2(p0, p1);
-                lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
-              }
-              tmem_st16(s_col + 32 * q, hi);
-              tmem_st16(s_col + 32 * q + 16, lo);
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              fma2(__uint_as_float(v0[32 * q + 2 * e]), __uint_as_float(v0[32 * q + 2 * e + 1]), a.scale_log2,
+                   neg_mu, x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(sum2x, p0, p1);
+              hi[e] = pack_bf16x2(p0, p1);
             }
+            tmem_st16(s_col + 16 * q, hi);
+          } else {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              fma2(__uint_as_float(v0[32 * q + 2 * e]), __uint_as_float(v0[32 * q + 2 * e + 1]), a.scale_log2,
+                   neg_mu, x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(sum2x, p0, p1);
+              hi[e] = pack_bf16x2(p0, p1);
+              lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
+            }
+            tmem_st16(s_col + 32 * q, hi);
+            tmem_st16(s_col + 32 * q + 16, lo);
           }
         }
         l = l * alpha + sum2(sum2x);
