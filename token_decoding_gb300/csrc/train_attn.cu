@@ -76,8 +76,15 @@ struct Cfg {
   static constexpr int V_OFF = K_OFF + NS * KV_BYTES;
   static constexpr int O_OFF = V_OFF + NS * KV_BYTES;  // per softmax warp: one [32 rows x 64] SW128 box
   static constexpr int SMEM = O_OFF + 8 * kOBox + 1024;  // + slack to align the base to 1024
-  static constexpr int TMEM_COLS = 512;                      // S_A | S_B | O_A | O_B
-  static constexpr int O_COL = 2 * kBN;
+  static constexpr int TMEM_COLS = 512;
+  // D = 64 keeps P apart from S (S_A | S_B | P_A | P_B | O_A | O_B), so the next S of a
+  // warpgroup is computed while its softmax still works on the current tile.  At
+  // D = 128 there is no room for it: P is written over S (S_A | S_B | O_A | O_B).
+  static constexpr bool SEPP = D == 64;
+  static constexpr int P_COL = 2 * kBN;  // P_x at P_COL + x * kBN / 2 (bf16 pairs), SEPP only
+  static constexpr int O_COL = SEPP ? 3 * kBN : 2 * kBN;
+  static_assert(!SEPP || O_COL + 2 * D <= TMEM_COLS, "tensor memory layout");
+  static_assert(NS >= 2, "the next key tile is awaited before the current tile's stage is released");
 };
 
 struct TrainArgs {
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_k[C::NS], bar_v[C::NS], bar_kv_empty[C::NS],
-      bar_s[2], bar_p[2], bar_o[2];
+      bar_s[2], bar_p[2], bar_o[2], bar_sfree[2], bar_pfree[2];
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_s[x], 1);
       mbar_init(&bar_p[x], 128);
       mbar_init(&bar_o[x], 1);
+      mbar_init(&bar_sfree[x], 128);  // SEPP: S_x has been read into registers
+      mbar_init(&bar_pfree[x], 1);    // SEPP: the PV that read P_x is complete
     }
     fence_mbar_init();
   }
@@ -332,7 +341,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      for (int idx; ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
+      // SEPP schedule: S_x(n + 1) as soon as the softmax has read S_x(n), then PV_x(n)
+      // from the separate P_x (a split tile is two PVs through P_x: hi, then lo).
+      int gs[2] = {0, 0};  // S products issued per query tile (SEPP)
+      auto issue_s_sep = [&](int x, int st) {
+        if (gs[x] > 0) {
+          wait_all(&bar_sfree[x], (gs[x] - 1) & 1);
+          if (!ok) return;
+          tc_fence_after();
+        }
+        ++gs[x];
+        issue_qk(x, st);
+      };
+      auto issue_pv_sep = [&](int x, int st, bool first, bool split) {
+        const uint32_t p_col = tmem + C::P_COL + x * (kBN / 2);
+        const uint32_t o_col = tmem + C::O_COL + x * D;
+        const uint64_t vb = desc_v + ((st * C::KV_BYTES) >> 4);
+        for (int part = 0; part < (split ? 2 : 1); ++part) {
+          wait_all(&bar_p[x], cp[x] & 1);
+          if (!ok) return;
+          ++cp[x];
+          tc_fence_after();
+          if (leader) {
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              tc_mma_ts(o_col, p_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv,
+                        (first && part == 0 && ks == 0) ? 0u : 1u);
+            tc_commit(&bar_pfree[x]);
+          }
+          __syncwarp();
+        }
+      };
+      for (int idx; C::SEPP && ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
+        const Item it = item_of(a, idx);
+        const int nt = it.sched.count();
+        wait_all(&bar_q_full, t & 1);
+        wait_all(&bar_k[kt % C::NS], (kt / C::NS) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s_sep(0, kt % C::NS);
+        if (it.two_q) issue_s_sep(1, kt % C::NS);
+        if (!ok) break;
+        if (nt == 1) commit(&bar_q_empty);
+        for (int n = 0; ok && n < nt; ++n, ++kt) {
+          const int st = kt % C::NS, st1 = (kt + 1) % C::NS;
+          const bool last = n + 1 == nt;
+          int kstart;
+          bool nz, part;
+          it.sched.at(n, kstart, nz, part);
+          const bool split = part && it.j == 0;  // same rule as the softmax warps
+          if (!last) {
+            wait_all(&bar_k[st1], ((kt + 1) / C::NS) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s_sep(0, st1);
+            if (it.two_q) issue_s_sep(1, st1);
+            if (!ok) break;
+            if (n + 2 == nt) commit(&bar_q_empty);  // the item's last S products are issued
+          }
+          wait_all(&bar_v[st], (kt / C::NS) & 1);
+          if (!ok) break;
+          issue_pv_sep(0, st, n == 0, split);
+          if (!ok) break;
+          if (last) commit(&bar_o[0]);
+          if (it.two_q) {
+            issue_pv_sep(1, st, n == 0, split);
+            if (!ok) break;
+            if (last) commit(&bar_o[1]);
+          }
+          commit(&bar_kv_empty[st]);
+        }
+      }
+      for (int idx; !C::SEPP && ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
         const Item it = item_of(a, idx);
         const int nt = it.sched.count();
         wait_all(&bar_q_full, t & 1);
@@ -383,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_col = tmem + lane_addr + x * kBN;
     const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
     int cs = 0, co = 0;  // S-ready and O-ready phases consumed
+    int cpw = 0;         // P_x writes (SEPP), one per P-ready phase
     bool ok = true;
     for (int t = 0, idx; ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
       const Item it = item_of(a, idx);
@@ -424,6 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kBN; c += 32) tmem_ld32(s_col + c, *reinterpret_cast<uint32_t(*)[32]>(&v0[c]));
         tc_wait_ld();
+        if constexpr (C::SEPP) {
+          tc_fence_before();
+          mbar_arrive(&bar_sfree[x]);  // S_x is in registers: the next S may overwrite it
+        }
         if (part) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c) v0[c] = (c >= vlo && c <= vhi) ? v0[c] : 0xFF800000u;
@@ -445,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = fast_exp2(m_used - tile_max);  // 0 when m_used is -inf
           m_used = tile_max;
         }
-        if (n > 0 && __any_sync(0xffffffffu, grow)) {
+        auto rescale_o = [&]() {
 #pragma unroll 1
           for (int c = 0; c < D; c += 16) {
             uint32_t ov[16];
@@ -455,8 +540,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
             tmem_st16(o_col + c, ov);
           }
-        }
+        };
         const float neg_mu = m_used == -INFINITY ? 0.f : -m_used;
+        if constexpr (C::SEPP) {
+          // P in registers first (PV_x of the previous tile may still be reading P_x),
+          // then wait for that PV, rescale O if the max grew, and store P_x: keys
+          // [32q, 32q + 32) -> columns [16q, 16q + 16).  A split tile stores hi, waits for
+          // its PV, then stores lo.
+          const uint32_t p_col = tmem + lane_addr + C::P_COL + x * (kBN / 2);
+          uint64_t sum2x = 0;
+          if (!split) {
+            uint32_t hi[kBN / 2];
+#pragma unroll
+            for (int e = 0; e < kBN / 2; ++e) {
+              float x0, x1;
+              fma2(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]), a.scale_log2, neg_mu, x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(sum2x, p0, p1);
+              hi[e] = pack_bf16x2(p0, p1);
+            }
+            if (cpw > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree[x], (cpw - 1) & 1));
+              if (!ok) break;
+            }
+            tc_fence_after();
+            if (n > 0 && __any_sync(0xffffffffu, grow)) rescale_o();
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q)
+              tmem_st16(p_col + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&hi[16 * q]));
+          } else {
+            if (cpw > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree[x], (cpw - 1) & 1));
+              if (!ok) break;
+            }
+            tc_fence_after();
+            if (n > 0 && __any_sync(0xffffffffu, grow)) rescale_o();
+            uint32_t lo[kBN / 2];
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q) {
+              uint32_t hq[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float x0, x1;
+                fma2(__uint_as_float(v0[32 * q + 2 * e]), __uint_as_float(v0[32 * q + 2 * e + 1]), a.scale_log2,
+                     neg_mu, x0, x1);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                add2(sum2x, p0, p1);
+                hq[e] = pack_bf16x2(p0, p1);
+                lo[16 * q + e] = pack_bf16x2(p0 - bf16lo_to_f32(hq[e]), p1 - bf16hi_to_f32(hq[e]));
+              }
+              tmem_st16(p_col + 16 * q, hq);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar_p[x]);  // hi
+            ++cpw;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree[x], (cpw - 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q)
+              tmem_st16(p_col + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&lo[16 * q]));
+          }
+          l = l * alpha + sum2(sum2x);
+          tc_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar_p[x]);  // P (non-split) or lo (split)
+          ++cpw;
+          continue;
+        }
+        if (n > 0 && __any_sync(0xffffffffu, grow)) rescale_o();
         // P = exp2(s * scale_log2 - mu) as bf16 pairs, written over S columns already read:
         // keys [32q, 32q + 32) -> hi in columns [16q, 16q + 16); on split tiles hi in
         // [32q, 32q + 16) and lo = P - hi in [32q + 16, 32q + 32).
