@@ -271,12 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           int kstart;
           bool nz, part;
           it.sched.at(n, kstart, nz, part);
-          mbar_arrive_expect_tx(&bar_k[st], C::KV_BYTES);
+          // SEPP: K and V of the stage both complete bar_k (one wait before its S);
+          // otherwise V has its own barrier, awaited just before the PV
+          uint64_t* bv = C::SEPP ? &bar_k[st] : &bar_v[st];
+          mbar_arrive_expect_tx(&bar_k[st], C::SEPP ? 2 * C::KV_BYTES : C::KV_BYTES);
           for (int c = 0; c < C::NB; ++c)
             tma_load_4d(k_s + st * C::KV_BYTES + c * kBox, &tm_k, &bar_k[st], 64 * c, it.g, kstart, it.b);
-          mbar_arrive_expect_tx(&bar_v[st], C::KV_BYTES);
+          if (!C::SEPP) mbar_arrive_expect_tx(bv, C::KV_BYTES);
           for (int c = 0; c < C::NB; ++c)
-            tma_load_4d(v_s + st * C::KV_BYTES + c * kBox, &tm_v, &bar_v[st], 64 * c, it.g, kstart, it.b);
+            tma_load_4d(v_s + st * C::KV_BYTES + c * kBox, &tm_v, bv, 64 * c, it.g, kstart, it.b);
         }
         if (!ok) break;
       }
@@ -399,9 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (n + 2 == nt) commit(&bar_q_empty);  // the item's last S products are issued
           }
-          wait_all(&bar_v[st], (kt / C::NS) & 1);
-          if (!ok) break;
-          issue_pv_sep(0, st, n == 0, split);
+          issue_pv_sep(0, st, n == 0, split);  // V(n) arrived with K(n), awaited before S(n)
           if (!ok) break;
           if (last) commit(&bar_o[0]);
           if (it.two_q) {
