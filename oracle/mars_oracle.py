@@ -48,6 +48,7 @@ __all__ = [
     "mask_rows",
     "mars_mask",
     "train_attn",
+    "train_attn_bwd",
     "decode_attn",
     "decode_attn_deferred",
     "accept_rows",
@@ -141,6 +142,47 @@ def train_attn(q, k, v, L: int, B: int, scale: float, rows=None):
             scores = scale * (q[b, rows, h, :] @ k[b, :, g, :].T)
             out[b, :, h, :], lse[b, h, :] = _softmax_attend(scores, visible, v[b, :, g, :])
     return out, lse
+
+
+def train_attn_bwd(q, k, v, do, L: int, B: int, scale: float):
+    """Gradients of the MARS masked attention (the forward of train_attn) with
+    respect to q, k and v, given the output gradient do ([paper] Sec. 3.2: both
+    streams share one forward, so one backward carries the gradients of
+    Eqs. 3 and 5 to q, k and v).
+
+    For one head, with S = scale * q k^T, P = softmax(S + M) over visible keys
+    and O = P v, the gradients are the textbook ones:
+        dV = P^T dO,   dP = dO v^T,
+        dS = P * (dP - rowsum(P * dP))       (the softmax Jacobian, row by row),
+        dQ = scale * dS k,   dK = scale * dS^T q.
+    With GQA every query head of a group adds its dK and dV to the group's KV
+    head.  q, do: [b, 2L, Hq, D]; k, v: [b, 2L, Hkv, D].
+    Returns (dq [b, 2L, Hq, D], dk [b, 2L, Hkv, D], dv [b, 2L, Hkv, D]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    nb, n2, hq, d = q.shape
+    hkv = k.shape[2]
+    assert n2 == 2 * L and k.shape == (nb, n2, hkv, d) and v.shape == k.shape and do.shape == q.shape
+    group = hq // hkv
+    visible = mars_mask(L, B)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(nb):
+        for h in range(hq):
+            g = h // group
+            s = np.where(visible, scale * (q[b, :, h, :] @ k[b, :, g, :].T), -np.inf)
+            e = np.exp(s - s.max(axis=1, keepdims=True))
+            p = e / e.sum(axis=1, keepdims=True)
+            dp = do[b, :, h, :] @ v[b, :, g, :].T
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            dv[b, :, g, :] += p.T @ do[b, :, h, :]
+            dq[b, :, h, :] = scale * (ds @ k[b, :, g, :])
+            dk[b, :, g, :] += scale * (ds.T @ q[b, :, h, :])
+    return dq, dk, dv
 
 
 # --------------------------------------------------------------------------

@@ -239,6 +239,94 @@ def check_train_block_ge_L(train_attn):
     assert np.max(np.abs(o[0, L:, 0] - ref)) < 1e-12
 
 
+# --------------------------------------------------------------------------
+# training attention backward pins
+# --------------------------------------------------------------------------
+
+def _autograd_bwd(q, k, v, do, L, B, scale):
+    """dq, dk, dv of sum(O * dO) by torch autograd (float64) through a dense
+    attention whose mask is the block construction above (not Eq. 2's cases)."""
+    import torch
+
+    nb, n2, hq, d = q.shape
+    hkv = k.shape[2]
+    group = hq // hkv
+    allowed = torch.from_numpy(mask_from_blocks(L, B))
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    loss = 0.0
+    for b in range(nb):
+        for h in range(hq):
+            g = h // group
+            s = (tq[b, :, h, :] @ tk[b, :, g, :].T) * scale
+            p = torch.softmax(s.masked_fill(~allowed, float("-inf")), dim=1)
+            loss = loss + ((p @ tv[b, :, g, :]) * torch.from_numpy(do[b, :, h, :])).sum()
+    loss.backward()
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def check_bwd_vs_autograd(train_attn_bwd):
+    for (nb, L, B, hq, hkv, d) in [(2, 12, 3, 4, 2, 8), (1, 13, 4, 3, 1, 6), (1, 7, 8, 2, 2, 4)]:
+        q, k, v = rand((nb, 2 * L, hq, d), 60), rand((nb, 2 * L, hkv, d), 61), rand((nb, 2 * L, hkv, d), 62)
+        do = rand((nb, 2 * L, hq, d), 63)
+        scale = d ** -0.5
+        got = train_attn_bwd(q, k, v, do, L, B, scale)
+        want = _autograd_bwd(q, k, v, do, L, B, scale)
+        for g_, w_ in zip(got, want):
+            assert np.max(np.abs(g_ - w_)) < 1e-11, np.max(np.abs(g_ - w_))
+
+
+def check_bwd_finite_differences(train_attn_bwd, train_attn):
+    """Central differences of sum(O * dO) through the (independently pinned) forward."""
+    L, B, d = 5, 2, 4
+    q, k, v = rand((1, 2 * L, 2, d), 64), rand((1, 2 * L, 1, d), 65), rand((1, 2 * L, 1, d), 66)
+    do = rand((1, 2 * L, 2, d), 67)
+    scale = 0.7
+    dq, dk, dv = train_attn_bwd(q, k, v, do, L, B, scale)
+    f = lambda q_, k_, v_: float(np.sum(train_attn(q_, k_, v_, L, B, scale)[0] * do))  # noqa: E731
+    eps = 1e-6
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        base = [q, k, v]
+        x = base[which]
+        for idx in [(0, 0, 0, 0), (0, 3, 0, 1), (0, 2 * L - 1, 0, 3), (0, L + 1, 0, 2), (0, L - 1, 0, 0)]:
+            if idx[2] >= x.shape[2]:
+                continue
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p, args_m = list(base), list(base)
+            args_p[which], args_m[which] = xp, xm
+            fd = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-7, (which, idx, fd, grad[idx])
+
+
+def check_bwd_gqa_is_repeat_kv(train_attn_bwd):
+    """dK, dV of a KV head are the sums over its query heads of the per-head gradients."""
+    L, B, d, hq, hkv = 9, 3, 8, 6, 2
+    q, k, v = rand((1, 2 * L, hq, d), 68), rand((1, 2 * L, hkv, d), 69), rand((1, 2 * L, hkv, d), 70)
+    do = rand((1, 2 * L, hq, d), 71)
+    dq, dk, dv = train_attn_bwd(q, k, v, do, L, B, 0.4)
+    kr, vr = np.repeat(k, hq // hkv, axis=2), np.repeat(v, hq // hkv, axis=2)
+    dq2, dk2, dv2 = train_attn_bwd(q, kr, vr, do, L, B, 0.4)
+    assert np.max(np.abs(dq - dq2)) < 1e-12
+    assert np.max(np.abs(dk - dk2.reshape(1, 2 * L, hkv, hq // hkv, d).sum(axis=3))) < 1e-12
+    assert np.max(np.abs(dv - dv2.reshape(1, 2 * L, hkv, hq // hkv, d).sum(axis=3))) < 1e-12
+
+
+def check_bwd_closed_forms(train_attn_bwd):
+    """Each row of P sums to 1, so the keys' dV rows sum to the rows of dO; a query
+    that sees a single key (z position 0, and the first placeholder of block 1) has
+    an all-zero softmax Jacobian, so its dQ row is exactly zero."""
+    L, B, d = 10, 4, 8
+    q, k, v = rand((2, 2 * L, 2, d), 72), rand((2, 2 * L, 1, d), 73), rand((2, 2 * L, 1, d), 74)
+    do = rand((2, 2 * L, 2, d), 75)
+    dq, dk, dv = train_attn_bwd(q, k, v, do, L, B, 0.35)
+    assert np.max(np.abs(dv.sum(axis=1)[:, 0, :] - do.sum(axis=(1, 2)))) < 1e-12
+    assert np.all(dq[:, 0] == 0) and np.all(dq[:, L] == 0)
+    assert np.all(dq[:, 1] != 0)
+
+
 def check_train_gqa_is_repeat_kv(train_attn):
     """Query head h uses KV head h // (Hq/Hkv): same as repeating each KV head
     Hq/Hkv times in a row (the Hugging Face repeat_kv layout)."""

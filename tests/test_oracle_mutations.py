@@ -53,6 +53,10 @@ def all_pins(m):
         "deferred_causal": lambda: pins.check_deferred_pending_rows_are_causal(m.decode_attn_deferred, m.train_attn),
         "deferred_invalid": lambda: pins.check_deferred_invalid_slots(m.decode_attn_deferred),
         "accept_deferred": lambda: pins.check_accept_deferred(m.accept_deferred, m.accept),
+        "bwd_autograd": lambda: pins.check_bwd_vs_autograd(m.train_attn_bwd),
+        "bwd_fd": lambda: pins.check_bwd_finite_differences(m.train_attn_bwd, m.train_attn),
+        "bwd_gqa": lambda: pins.check_bwd_gqa_is_repeat_kv(m.train_attn_bwd),
+        "bwd_closed": lambda: pins.check_bwd_closed_forms(m.train_attn_bwd),
     }
     failed = []
     for name, fn in checks.items():
@@ -113,6 +117,16 @@ MUTATIONS = [
     # deferred acceptance advancing by the new count instead of the pending one
     ("np.asarray(cache_len, dtype=np.int64) + np.asarray(pending, dtype=np.int64)",
      "np.asarray(cache_len, dtype=np.int64) + n"),
+    # backward: the softmax Jacobian without its row-sum term
+    ("            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))", "            ds = p * dp"),
+    # backward: dQ without the scale
+    ("            dq[b, :, h, :] = scale * (ds @ k[b, :, g, :])", "            dq[b, :, h, :] = ds @ k[b, :, g, :]"),
+    # backward: dV from P instead of its transpose
+    ("            dv[b, :, g, :] += p.T @ do[b, :, h, :]", "            dv[b, :, g, :] += p @ do[b, :, h, :]"),
+    # backward: GQA heads overwrite instead of adding into dK
+    ("            dk[b, :, g, :] += scale * (ds.T @ q[b, :, h, :])", "            dk[b, :, g, :] = scale * (ds.T @ q[b, :, h, :])"),
+    # backward: dP against K instead of V
+    ("            dp = do[b, :, h, :] @ v[b, :, g, :].T", "            dp = do[b, :, h, :] @ k[b, :, g, :].T"),
     # batch-minimum mode taking the maximum
     ("n = np.full_like(n, n.min())", "n = np.full_like(n, n.max())"),
     # strict > instead of >= tau

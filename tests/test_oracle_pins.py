@@ -151,3 +151,19 @@ def test_accept_rejects_non_finite():
 def test_near_threshold_band():
     flags = oracle.near_threshold(np.array([0.95, 0.95005, 0.9502, 0.94991]), 0.95)
     assert list(flags) == [True, True, False, True]
+
+
+def test_bwd_vs_autograd():
+    pins.check_bwd_vs_autograd(oracle.train_attn_bwd)
+
+
+def test_bwd_finite_differences():
+    pins.check_bwd_finite_differences(oracle.train_attn_bwd, oracle.train_attn)
+
+
+def test_bwd_gqa_is_repeat_kv():
+    pins.check_bwd_gqa_is_repeat_kv(oracle.train_attn_bwd)
+
+
+def test_bwd_closed_forms():
+    pins.check_bwd_closed_forms(oracle.train_attn_bwd)
