@@ -454,6 +454,9 @@ def run_gpu(args, rank, world, local):
     # the deferred-KV sampler (decode over 2B slots with the fused commit, then the
     # acceptance that only moves the cursor), timed the same way
     parts.update(run_deferred_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic, gen))
+    # the backward of the training-mask attention on both training shapes
+    parts["train_bwd_05b"] = run_train_bwd(args, mars, train05, peaks["bf16_tflops"], traffic, "train_bwd_05b")
+    parts["train_bwd_7b"] = run_train_bwd(args, mars, train7, peaks["bf16_tflops"], traffic, "train_bwd_7b")
 
     line = {
         "metric": METRIC,
@@ -618,6 +621,42 @@ def run_deferred_variant(args, mars, work, device, hbm_peak, traffic, gen):
     }
 
 
+def run_train_bwd(args, mars, work, peak, traffic, name):
+    """mars_train_attn_bwd on a training shape: min(steps, 20) calls over the rotating
+    input sets (their o and lse from one forward each), CUDA events on the stream.
+    Useful FLOPs = 2.5 x the forward's: five products (S, dP, dV, dK, dQ) over the
+    visible pairs; the kernels also recompute S and dP for dQ, which is not counted."""
+    import torch
+
+    s = work.s
+    n = max(1, min(args.steps, 20))
+    stream = torch.cuda.current_stream()
+    prep = []
+    for q, k, v, _ in work.sets:
+        o_, lse = mars.train_attn(q, k, v, s.L, s.B, want_lse=True)
+        do = torch.randn(q.shape, device=q.device, dtype=torch.float32).to(torch.bfloat16)
+        prep.append((q, k, v, o_, do, lse, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)))
+    ws = torch.empty(s.batch * s.Hq * 2 * s.L * 4 + 256, dtype=torch.uint8, device=prep[0][0].device)
+
+    def call(i):
+        q, k, v, o_, do, lse, dq, dk, dv = prep[i % len(prep)]
+        mars.train_attn_bwd(q, k, v, o_, do, lse, s.L, s.B, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    achieved = 2.5 * work.flops / (ms * 1e-3) / 1e12
+    return {"avg_us": round(ms * 1e3, 3), "calls": n, "useful_tflop_per_call": round(2.5 * work.flops / 1e12, 4),
+            "roofline": roofline("tensor", achieved, peak, "TFLOP/s", traffic.get(name))}
+
+
 def run_graph(mars, work, device, hbm_peak):
     """A whole decode episode (decode attention + accept per step: 256 steps at batch 1,
     128 at batch 64) captured as one CUDA graph; device-side steps/s and the
@@ -744,7 +783,14 @@ def run_profile(args):
     gen = torch.Generator(device=device)
     gen.manual_seed(1234)
     part = args.profile
-    if part.startswith("train"):
+    if part.startswith("train_bwd"):
+        w = TrainWork(synth.TRAIN_05B if part == "train_bwd_05b" else synth.TRAIN_7B, device, gen, 0)
+        s = w.s
+        q, k, v, _ = w.sets[0]
+        o_, lse = mars.train_attn(q, k, v, s.L, s.B, want_lse=True)
+        do = torch.randn(q.shape, generator=gen, device=device).to(torch.bfloat16)
+        run = lambda i: mars.train_attn_bwd(q, k, v, o_, do, lse, s.L, s.B)  # noqa: E731
+    elif part.startswith("train"):
         w = TrainWork(synth.TRAIN_05B if part == "train_05b" else synth.TRAIN_7B, device, gen, 0)
         run = lambda i: w.run(mars, i)  # noqa: E731
     else:
@@ -798,7 +844,7 @@ def main():
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph decode episodes (batch 1 and 64)")
     p.add_argument("--profile", choices=["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1",
                                          "accept_b1", "accept_margin_b64", "decode_attn_deferred_b64",
-                                         "accept_deferred_b64"],
+                                         "accept_deferred_b64", "train_bwd_05b", "train_bwd_7b"],
                    help="only launch this kernel, warm-up + steps times, and print no JSON (for ncu)")
     args = p.parse_args()
     if args.steps is None:

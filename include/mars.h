@@ -49,7 +49,8 @@ extern "C" {
 #define MARS_DEV_CAPACITY 1   /* mars_accept: cache_len + n_commit would exceed cap; that sequence was not appended;
                                  mars_decode_attn_deferred: cache_len + pending > cap; that sequence's output is zero */
 #define MARS_DEV_LEN_RANGE 2  /* mars_decode_attn: a cache_len[b] was < 0 or > max_len; that sequence's output is zero */
-#define MARS_DEV_TIMEOUT 4    /* mars_train_attn: an internal pipeline wait hit its iteration limit; output incomplete */
+#define MARS_DEV_TIMEOUT 4    /* mars_train_attn(_bwd), mars_decode_attn, mars_accept: an internal pipeline wait hit
+                                 its iteration limit; output incomplete */
 
 /* Human-readable text for a return code (static storage, never NULL). */
 const char* mars_status_string(int status);
@@ -84,6 +85,38 @@ int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     uint16_t* o, float* lse,
                     int batch, int L, int B, int Hq, int Hkv, int D, float scale,
                     int32_t* status, void* stream);
+
+/*
+ * mars_train_attn_bwd - gradients of mars_train_attn with respect to q, k and
+ * v ([paper] Sec. 3.2: both streams share one forward, so one backward carries
+ * the gradients of the training losses, Eqs. 3 and 5, to q, k and v).
+ *
+ * For every head, with S = scale q k^T, P = softmax(S + M) (the Eq. 2 mask,
+ * recomputed from the forward's log-sum-exp: P = exp(S - lse)) and dO the
+ * gradient of o:
+ *   dV = P^T dO,  dP = dO v^T,  dS = P * (dP - rowsum(dO * o)),
+ *   dQ = scale dS k,  dK = scale dS^T q,
+ * and with GQA every query head of a group adds its dK, dV to the group's KV
+ * head.  P and dS are rounded to bf16 for the tensor-core products, every
+ * accumulation is fp32, the outputs are bf16.
+ *
+ *   q, o, dout [batch, 2L, Hq, D] bf16        dq [batch, 2L, Hq, D] bf16 (written)
+ *   k, v       [batch, 2L, Hkv, D] bf16       dk, dv [batch, 2L, Hkv, D] bf16 (written)
+ *   lse        [batch, Hq, 2L] fp32 (the forward's, natural log)
+ *   workspace  device buffer of >= mars_train_attn_bwd_workspace_size(batch,
+ *              L, Hq) bytes (it holds rowsum(dO * o)); contents on entry do not
+ *              matter; calls that share it must not overlap in time.
+ * Three kernel launches on `stream` (the row sums, then dK and dV over key
+ * tiles, then dQ over query tiles); no atomics, so the result is
+ * deterministic.  Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= B;
+ * 1 <= L <= 65536.  All pointers 16-byte aligned except lse (4 bytes).
+ */
+size_t mars_train_attn_bwd_workspace_size(int batch, int L, int Hq);
+int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const uint16_t* o, const uint16_t* dout, const float* lse,
+                        uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                        int batch, int L, int B, int Hq, int Hkv, int D, float scale,
+                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * mars_decode_attn - attention of one sliding-window decode step

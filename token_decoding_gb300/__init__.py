@@ -18,5 +18,6 @@ from ._lib import (  # noqa: F401
     lib,
     status_string,
     train_attn,
+    train_attn_bwd,
     version,
 )

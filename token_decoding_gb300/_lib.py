@@ -42,6 +42,8 @@ _SIGNATURES = {
     "mars_version": (_I, []),
     "mars_last_cuda_error": (ctypes.c_char_p, []),
     "mars_train_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "mars_train_attn_bwd_workspace_size": (_SZ, [_I, _I, _I]),
+    "mars_train_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_decode_attn_deferred": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
@@ -158,6 +160,40 @@ def train_attn(q, k, v, L: int, B: int, scale: float | None = None, o=None, lse=
     _call("mars_train_attn", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), nb, L, B, hq, hkv, d, float(scale),
           _ptr(status), _stream(stream))
     return (o, lse) if lse is not None else o
+
+
+def train_attn_bwd(q, k, v, o, dout, lse, L: int, B: int, scale: float | None = None, dq=None, dk=None, dv=None,
+                   workspace=None, status=None, stream=None):
+    """Gradients of train_attn (include/mars.h: mars_train_attn_bwd).
+
+    q, o, dout [b, 2L, Hq, D], k, v [b, 2L, Hkv, D] bf16; lse [b, Hq, 2L] fp32
+    from the forward.  Returns (dq, dk, dv) in the shapes of q, k, v."""
+    nb, n2, hq, d = q.shape
+    hkv = k.shape[2]
+    dev = q.device
+    _check(q, "q", torch.bfloat16, (nb, 2 * L, hq, d))
+    for t, name in ((o, "o"), (dout, "dout")):
+        _check(t, name, torch.bfloat16, q.shape, dev)
+    _check(k, "k", torch.bfloat16, (nb, 2 * L, hkv, d), dev)
+    _check(v, "v", torch.bfloat16, (nb, 2 * L, hkv, d), dev)
+    _check(lse, "lse", torch.float32, (nb, hq, 2 * L), dev)
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(dq, "dq", torch.bfloat16, q.shape, dev)
+    _check(dk, "dk", torch.bfloat16, k.shape, dev)
+    _check(dv, "dv", torch.bfloat16, v.shape, dev)
+    if workspace is None:
+        n = int(_fn("mars_train_attn_bwd_workspace_size")(nb, L, hq))
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_train_attn_bwd", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+          _ptr(dv), nb, L, B, hq, hkv, d, float(scale), _ptr(workspace), workspace.numel(), _ptr(status),
+          _stream(stream))
+    return dq, dk, dv
 
 
 def decode_attn(q, k_new, v_new, k_cache, v_cache, cache_len, max_len: int, scale: float | None = None, o=None,

@@ -1,0 +1,544 @@
+// train_attn_bwd.cu - mars_train_attn_bwd: dQ, dK, dV of the MARS masked
+// attention over z = [x ; x~].
+//
+// Method: "MARS: Enabling Autoregressive Models Multi-Token Generation",
+// Sec. 3.2 (Eq. 1, Eq. 2: both streams share one forward, so one backward
+// carries the gradients of the losses of Eqs. 3 and 5 to q, k and v).  For one
+// head, with S = scale q k^T, P = softmax(S + M) and O = P v:
+//   dV = P^T dO,  dP = dO v^T,  dS = P * (dP - delta),  delta_i = sum_d dO_i O_i,
+//   dQ = scale dS k,  dK = scale dS^T q,
+// and P is recomputed from the forward's log-sum-exp: P = exp(S - lse).
+//
+// sm_103a design (tensor-bound).  Three launches, no atomics, deterministic:
+//   1. delta_kernel: delta_i = rowsum(dO_i * O_i), fp32, one warp per row.
+//   2. bwd_kernel<kDKV>: one CTA per (sequence, KV head, 128-key tile).  For
+//      every query head of the group and every 128-row query tile that sees
+//      the key tile (an exact interval test on Eq. 2's structure), tcgen05
+//      computes S = Q K^T and dP = dO V^T into tensor memory; four warps (one
+//      query row per thread) form P and dS and write them to shared memory as
+//      SW128 [128 rows x 64 keys] tiles; tcgen05 then accumulates dV += P^T dO
+//      and dK += dS^T Q in tensor memory (the P / dS tiles are read MN-major
+//      as the A operand, Q / dO MN-major as B).
+//   3. bwd_kernel<kDQ>: one CTA per (sequence, query head, 128-row query tile):
+//      the same S, dP, dS steps for every key tile the query tile sees, then
+//      dQ += dS K (dS K-major, K MN-major).
+// Roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one elected lane),
+// warps 2..5 elementwise (thread = TMEM lane = query row).  Every mbarrier wait
+// is bounded; a wait that gives up sets MARS_DEV_TIMEOUT.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace mars;
+
+constexpr int kT = 128;            // query rows of a query tile = keys of a key tile
+constexpr int kBox = 128 * 128;    // bytes of one [128 rows x 64 bf16] SW128 box
+constexpr int kThreads = 192;      // producer, MMA issuer, 4 elementwise warps
+constexpr int kMaxTiles = 1024;    // tiles per batch entry and head (2 * ceil(L / 128))
+
+enum Mode { kDKV = 0, kDQ = 1 };
+
+template <int D, int MODE>
+struct BCfg {
+  static constexpr int NB = D / 64;
+  static constexpr int TILE = NB * kBox;  // one [128 x D] bf16 tile
+  // dKV: the unit's K and V once, Q and dO in NS stages.  dQ: the unit's Q and
+  // dO once, K and V in NS stages.  Both: P (dKV only) and dS [128 x 128] tiles.
+  static constexpr int NS = (MODE == kDKV && D == 128) ? 1 : 2;  // 256 KB would not fit at D = 128
+  static constexpr int FIXED_OFF = 0;                   // K, V (dKV) or Q, dO (dQ)
+  static constexpr int RING_OFF = FIXED_OFF + 2 * TILE;  // stage s: Q, dO (dKV) or K, V (dQ)
+  static constexpr int P_OFF = RING_OFF + NS * 2 * TILE;
+  static constexpr int DS_OFF = P_OFF + (MODE == kDKV ? 2 * kBox : 0);
+  static constexpr int SMEM = DS_OFF + 2 * kBox + 1024;  // + slack to align the base to 1024
+  static constexpr int S_COL = 0, DP_COL = kT, ACC_COL = 2 * kT;  // ACC: dK | dV, or dQ
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(ACC_COL + (MODE == kDKV ? 2 : 1) * D <= 512, "tensor memory");
+};
+
+struct UnitOrder {
+  uint16_t tile[kMaxTiles];  // tile indices (0 .. 2 * nt - 1), heaviest first
+};
+
+struct BwdArgs {
+  const float* lse;    // [b, Hq, 2L] natural log
+  const float* delta;  // [b, Hq, 2L]
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  int32_t* status;
+  int batch, L, B, Hq, Hkv, G;
+  int nt;              // tiles per stream: ceil(L / 128)
+  float scale_log2;    // scale * log2(e)
+  float scale;
+};
+
+// Tile t of the 2 * nt tiles of z: stream t / nt, rows [r0, r0 + 128) cut at end.
+__host__ __device__ __forceinline__ void tile_rows(const BwdArgs& a, int t, int& r0, int& end) {
+  const bool noisy = t >= a.nt;
+  const int j = noisy ? t - a.nt : t;
+  r0 = (noisy ? a.L : 0) + kT * j;
+  end = noisy ? 2 * a.L : a.L;
+}
+
+// Does any query row of query tile qt see any key of key tile kt (Eq. 2)?
+__host__ __device__ __forceinline__ bool tile_visible(const BwdArgs& a, int qt, int kt) {
+  int q0, qe, k0, ke;
+  tile_rows(a, qt, q0, qe);
+  tile_rows(a, kt, k0, ke);
+  const int q1 = min(q0 + kT, qe) - 1, k1 = min(k0 + kT, ke) - 1;
+  if (q0 < a.L) return k0 < a.L && q1 >= k0;  // clean rows see the clean causal prefix
+  // noisy rows t = i - L see clean [0, B * (t / B) - 1] and noisy [L + B * (t / B), i]
+  if (k0 < a.L) return a.B * ((q1 - a.L) / a.B) - 1 >= k0;
+  const int i = max(q0, k0);
+  return i <= q1 && a.L + a.B * ((i - a.L) / a.B) <= k1;
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // descriptor version for sm_100-class tensor cores
+  d |= 2ull << 61;  // 128-byte swizzle
+  return d;
+}
+
+// bf16 x bf16 -> fp32, M x N; a_mn / b_mn: the operand is MN-major (transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- delta
+__global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                    float* __restrict__ delta, int batch, int n2, int Hq, int D) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (b, i, h)
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(batch) * n2 * Hq) return;
+  const int h = static_cast<int>(row % Hq);
+  const long long bi = row / Hq;
+  const int i = static_cast<int>(bi % n2), b = static_cast<int>(bi / n2);
+  const uint16_t* po = o + row * D;
+  const uint16_t* pd = dout + row * D;
+  float acc = 0.f;
+  for (int c = 2 * lane; c < D; c += 64) {
+    const uint32_t wo = *reinterpret_cast<const uint32_t*>(po + c), wd = *reinterpret_cast<const uint32_t*>(pd + c);
+    acc = fmaf(bf16lo_to_f32(wo), bf16lo_to_f32(wd), acc);
+    acc = fmaf(bf16hi_to_f32(wo), bf16hi_to_f32(wd), acc);
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) delta[(static_cast<size_t>(b) * Hq + h) * n2 + i] = acc;
+}
+
+// ---------------------------------------------------------------- main kernel
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdArgs a,
+               const __grid_constant__ UnitOrder order) {
+  using C = BCfg<D, MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_fixed, bar_stage[C::NS], bar_free[C::NS], bar_s, bar_p, bar_acc;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- the unit: (b, g, key tile) for dKV, (b, h, query tile) for dQ; heaviest tiles first
+  const int ntiles = 2 * a.nt;
+  const int heads = MODE == kDKV ? a.Hkv : a.Hq;
+  const int per_tile = a.batch * heads;
+  const int tile = order.tile[blockIdx.x / per_tile];
+  const int rest = blockIdx.x % per_tile;
+  const int b = rest / heads, hh = rest % heads;  // hh: KV head (dKV) or query head (dQ)
+  int u0, uend;
+  tile_rows(a, tile, u0, uend);
+  // The steps of the unit: every (query head of the group, query tile) that sees the
+  // key tile (dKV), or every key tile the query tile sees (dQ), in index order.  Each
+  // role walks them with its own iterator.
+  const int nsteps_heads = MODE == kDKV ? a.G : 1;
+  struct Steps {
+    int hs = 0, t = -1;
+  };
+  auto next_step = [&](Steps& it, int& head, int& other) {
+    while (true) {
+      if (++it.t == ntiles) {
+        it.t = 0;
+        if (++it.hs == nsteps_heads) return;
+      }
+      if (MODE == kDKV ? tile_visible(a, it.t, tile) : tile_visible(a, tile, it.t)) break;
+    }
+    head = MODE == kDKV ? hh * a.G + it.hs : hh;
+    other = it.t;
+  };
+  int nsteps = 0;
+  for (int t = 0; t < ntiles; ++t) nsteps += (MODE == kDKV ? tile_visible(a, t, tile) : tile_visible(a, tile, t));
+  nsteps *= nsteps_heads;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_fixed, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bar_stage[s], 1);
+      mbar_init(&bar_free[s], 1);
+    }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_p, 128);
+    mbar_init(&bar_acc, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t fixed_s = smem_u32(smem + C::FIXED_OFF);
+  const uint32_t ring_s = smem_u32(smem + C::RING_OFF);
+  const uint32_t p_s = smem_u32(smem + C::P_OFF);
+  const uint32_t ds_s = smem_u32(smem + C::DS_OFF);
+  const int g = MODE == kDKV ? hh : hh / a.G;  // KV head
+  bool ok = true;
+
+  if (warp == 0) {
+    // ================= TMA producer
+    if (lane == 0) {
+      // fixed operands: K, V of the key tile (dKV) or Q, dO of the query tile (dQ)
+      mbar_arrive_expect_tx(&bar_fixed, 2 * C::TILE);
+      for (int c = 0; c < C::NB; ++c) {
+        if (MODE == kDKV) {
+          tma_load_4d(fixed_s + c * kBox, &tm_k, &bar_fixed, 64 * c, g, u0, b);
+          tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_v, &bar_fixed, 64 * c, g, u0, b);
+        } else {
+          tma_load_4d(fixed_s + c * kBox, &tm_q, &bar_fixed, 64 * c, hh, u0, b);
+          tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_do, &bar_fixed, 64 * c, hh, u0, b);
+        }
+      }
+      Steps sit;
+      for (int n = 0; n < nsteps; ++n) {
+        const int st = n % C::NS;
+        if (n >= C::NS && !mbar_wait(&bar_free[st], ((n / C::NS) - 1) & 1)) {
+          set_status(a.status, MARS_DEV_TIMEOUT);
+          break;
+        }
+        int head = 0, other = 0;
+        next_step(sit, head, other);
+        int o0, oe;
+        tile_rows(a, other, o0, oe);
+        const uint32_t dst = ring_s + st * 2 * C::TILE;
+        mbar_arrive_expect_tx(&bar_stage[st], 2 * C::TILE);
+        for (int c = 0; c < C::NB; ++c) {
+          if (MODE == kDKV) {
+            tma_load_4d(dst + c * kBox, &tm_q, &bar_stage[st], 64 * c, head, o0, b);
+            tma_load_4d(dst + C::TILE + c * kBox, &tm_do, &bar_stage[st], 64 * c, head, o0, b);
+          } else {
+            tma_load_4d(dst + c * kBox, &tm_k, &bar_stage[st], 64 * c, g, o0, b);
+            tma_load_4d(dst + C::TILE + c * kBox, &tm_v, &bar_stage[st], 64 * c, g, o0, b);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer (whole warp runs the schedule, one elected lane issues)
+    const bool leader = elect_one();
+    constexpr uint32_t id_s = idesc_bf16(kT, kT, false, false);   // S, dP: A, B K-major
+    constexpr uint32_t id_acc = MODE == kDKV ? idesc_bf16(kT, D, true, true)   // P^T dO, dS^T Q
+                                             : idesc_bf16(kT, D, false, true); // dS K
+    auto wait_all = [&](uint64_t* bar, int parity) { ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
+    wait_all(&bar_fixed, 0);
+    tc_fence_after();
+    for (int n = 0; ok && n < nsteps; ++n) {
+      const int st = n % C::NS;
+      wait_all(&bar_stage[st], (n / C::NS) & 1);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t stage = ring_s + st * 2 * C::TILE;
+      // Q and dO tiles: the fixed ones (dQ) or this step's (dKV); K and V the other way round
+      const uint32_t q_t = MODE == kDKV ? stage : fixed_s, do_t = q_t + C::TILE;
+      const uint32_t k_t = MODE == kDKV ? fixed_s : stage, v_t = k_t + C::TILE;
+      if (leader) {
+        const uint64_t dq_ = smem_desc(q_t, 16, 1024), dk_ = smem_desc(k_t, 16, 1024);
+        const uint64_t ddo = smem_desc(do_t, 16, 1024), dv_ = smem_desc(v_t, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
+          tc_mma_ss(tmem + C::S_COL, dq_ + off, dk_ + off, id_s, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
+          tc_mma_ss(tmem + C::DP_COL, ddo + off, dv_ + off, id_s, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&bar_s);
+      }
+      __syncwarp();
+      wait_all(&bar_p, n & 1);  // P and dS are in shared memory
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        if (MODE == kDKV) {
+          // dV += P^T dO and dK += dS^T Q over the 128 query rows (16 per step)
+          const uint64_t dpa = smem_desc(p_s, kBox, 1024), dsa = smem_desc(ds_s, kBox, 1024);
+          const uint64_t ddo = smem_desc(do_t, kBox, 1024), dqb = smem_desc(q_t, kBox, 1024);
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks) {
+            const uint32_t off = (ks * 16 * 128) >> 4;
+            tc_mma_ss(tmem + C::ACC_COL + D, dpa + off, ddo + off, id_acc, (n > 0 || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks) {
+            const uint32_t off = (ks * 16 * 128) >> 4;
+            tc_mma_ss(tmem + C::ACC_COL, dsa + off, dqb + off, id_acc, (n > 0 || ks > 0) ? 1u : 0u);
+          }
+        } else {
+          // dQ += dS K over the 128 keys (16 per step): dS K-major, K MN-major
+          const uint64_t dsa = smem_desc(ds_s, 16, 1024), dkb = smem_desc(k_t, kBox, 1024);
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks) {
+            const uint32_t aoff = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4, boff = (ks * 16 * 128) >> 4;
+            tc_mma_ss(tmem + C::ACC_COL, dsa + aoff, dkb + boff, id_acc, (n > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        tc_commit(&bar_free[st]);
+        if (n + 1 == nsteps) tc_commit(&bar_acc);
+      }
+      __syncwarp();
+    }
+    if (!ok && leader) set_status(a.status, MARS_DEV_TIMEOUT);
+    __syncwarp();
+  } else {
+    // ================= elementwise: thread = TMEM lane = row of S (a query row)
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    Steps sit;
+    for (int n = 0; n < nsteps; ++n) {
+      int head = 0, other = 0;
+      next_step(sit, head, other);
+      // query tile and key tile of this step
+      const int qt = MODE == kDKV ? other : tile, kt = MODE == kDKV ? tile : other;
+      int q0, qe, k0, ke;
+      tile_rows(a, qt, q0, qe);
+      tile_rows(a, kt, k0, ke);
+      const int i = q0 + r;
+      const bool row_ok = i < qe;
+      // visible keys of row i (Eq. 2): clean [0, c_hi], noisy [n_lo, n_hi]
+      int c_hi = -1, n_lo = 1, n_hi = 0;
+      if (row_ok) {
+        if (i < a.L) {
+          c_hi = i;
+        } else {
+          const int c = a.B * ((i - a.L) / a.B);
+          c_hi = c - 1;
+          n_lo = a.L + c;
+          n_hi = i;
+        }
+      }
+      const size_t ri = (static_cast<size_t>(b) * a.Hq + head) * (2 * a.L) + (row_ok ? i : 0);
+      const float lse2 = row_ok ? __ldg(a.lse + ri) * kLog2e : 0.f;
+      const float dlt = row_ok ? __ldg(a.delta + ri) : 0.f;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s, n & 1));
+      if (!ok) break;
+      tc_fence_after();
+      // (S(n) complete implies every earlier MMA is complete: the P / dS tiles are free)
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {  // keys [64 hb, 64 hb + 64): one SW128 box
+        uint32_t sv[64], dpv[64];
+        tmem_ld32(tmem + lane_addr + C::S_COL + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tmem + lane_addr + C::S_COL + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
+        tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+        tc_wait_ld();
+        const uint32_t row_off = static_cast<uint32_t>(hb * kBox + r * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // 8 keys = one 16-byte chunk
+          uint32_t pw[4], dw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pp[2], dd[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int c = 8 * q + 2 * e + u;
+              const int j = k0 + 64 * hb + c;
+              const bool vis = j < ke && (j <= c_hi || (j >= n_lo && j <= n_hi));
+              const float p = vis ? fast_exp2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -lse2)) : 0.f;
+              pp[u] = p;
+              dd[u] = p * (__uint_as_float(dpv[c]) - dlt);
+            }
+            pw[e] = pack_bf16x2(pp[0], pp[1]);
+            dw[e] = pack_bf16x2(dd[0], dd[1]);
+          }
+          const uint32_t sw = static_cast<uint32_t>(((q ^ (r & 7)) * 16));
+          if (MODE == kDKV) st_shared_v4(p_s + row_off + sw, pw[0], pw[1], pw[2], pw[3]);
+          st_shared_v4(ds_s + row_off + sw, dw[0], dw[1], dw[2], dw[3]);
+        }
+      }
+      fence_async_smem();  // the generic-proxy stores become visible to the tensor core
+      tc_fence_before();
+      mbar_arrive(&bar_p);
+    }
+    // ---- epilogue: the accumulators (rows = keys for dK, dV; query rows for dQ)
+    if (ok && nsteps > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc, 0));
+    if (!ok) {
+      if (lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const int row = u0 + r;
+      const bool store = row < uend;
+#pragma unroll 1
+      for (int m = 0; m < (MODE == kDKV ? 2 : 1); ++m) {
+        uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
+        const int H = MODE == kDKV ? a.Hkv : a.Hq;
+        const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
+        uint4* out = reinterpret_cast<uint4*>(dst + ((static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0)) * H + hh) * D);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
+          tc_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f) : 0u;
+          if (store) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) out[(c >> 3) + w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [batch, n, H, D] bf16 as a 4-D tensor loaded in [128 rows x 64 columns] SW128 boxes.
+bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(n) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kT), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tiles in decreasing order of the number of tiles on the other side they meet.
+void make_order(const BwdArgs& a, int mode, UnitOrder* o) {
+  const int n = 2 * a.nt;
+  std::vector<int> w(n, 0), idx(n);
+  for (int t = 0; t < n; ++t) {
+    idx[t] = t;
+    for (int u = 0; u < n; ++u) w[t] += mode == kDKV ? tile_visible(a, u, t) : tile_visible(a, t, u);
+  }
+  std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) { return w[x] > w[y]; });
+  for (int t = 0; t < n; ++t) o->tile[t] = static_cast<uint16_t>(idx[t]);
+}
+
+template <int D, int MODE>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+           const BwdArgs& a, cudaStream_t stream) {
+  using C = BCfg<D, MODE>;
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
+    configured = true;
+  }
+  UnitOrder order;
+  make_order(a, MODE, &order);
+  const long long units = 2LL * a.nt * a.batch * (MODE == kDKV ? a.Hkv : a.Hq);
+  bwd_kernel<D, MODE><<<static_cast<int>(units), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a, order);
+  return mars_host::launch_status();
+}
+
+inline size_t align_up(size_t x, size_t al) { return (x + al - 1) / al * al; }
+
+}  // namespace
+
+extern "C" size_t mars_train_attn_bwd_workspace_size(int batch, int L, int Hq) {
+  if (batch <= 0 || L <= 0 || Hq <= 0) return 0;
+  return align_up(static_cast<size_t>(batch) * Hq * 2 * L * sizeof(float), 256);
+}
+
+extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o,
+                                   const uint16_t* dout, const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                                   int batch, int L, int B, int Hq, int Hkv, int D, float scale, void* workspace,
+                                   size_t workspace_bytes, int32_t* status, void* stream) {
+  using mars_host::aligned16;
+  MARS_HOST_CHECK(batch > 0 && L > 0 && B > 0 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0, MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(D == 64 || D == 128, MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(scale > 0.f && scale < INFINITY, MARS_ERR_INVALID_ARG);
+  const int nt = (L + kT - 1) / kT;
+  MARS_HOST_CHECK(2 * nt <= kMaxTiles, MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(2LL * nt * batch * Hq < (1LL << 31), MARS_ERR_INVALID_ARG);
+  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void* p : ptrs) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(lse != nullptr && mars_host::aligned4(lse), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(status == nullptr || mars_host::aligned4(status), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(workspace != nullptr && aligned16(workspace), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(workspace_bytes >= mars_train_attn_bwd_workspace_size(batch, L, Hq), MARS_ERR_WORKSPACE_TOO_SMALL);
+  int rc = mars_host::check_device();
+  if (rc != MARS_OK) return rc;
+
+  BwdArgs a;
+  a.lse = lse;
+  a.delta = static_cast<const float*>(workspace);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = status;
+  a.batch = batch;
+  a.L = L;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.nt = nt;
+  a.scale_log2 = scale * kLog2e;
+  a.scale = scale;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, D, Hq, 2 * L, batch) || !make_map(&tk, k, D, Hkv, 2 * L, batch) ||
+      !make_map(&tv, v, D, Hkv, 2 * L, batch) || !make_map(&tdo, dout, D, Hq, 2 * L, batch))
+    return MARS_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
+  delta_kernel<<<static_cast<int>((rows + 7) / 8), 256, 0, s>>>(o, dout, static_cast<float*>(workspace), batch, 2 * L,
+                                                               Hq, D);
+  rc = mars_host::launch_status();
+  if (rc != MARS_OK) return rc;
+  rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, s);
+  if (rc != MARS_OK) return rc;
+  return D == 64 ? launch<64, kDQ>(tq, tk, tv, tdo, a, s) : launch<128, kDQ>(tq, tk, tv, tdo, a, s);
+}
