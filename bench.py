@@ -636,7 +636,8 @@ def run_train_bwd(args, mars, work, peak, traffic, name):
         o_, lse = mars.train_attn(q, k, v, s.L, s.B, want_lse=True)
         do = torch.randn(q.shape, device=q.device, dtype=torch.float32).to(torch.bfloat16)
         prep.append((q, k, v, o_, do, lse, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)))
-    ws = torch.empty(s.batch * s.Hq * 2 * s.L * 4 + 256, dtype=torch.uint8, device=prep[0][0].device)
+    ws = torch.empty(mars._lib.train_attn_bwd_workspace_size(s.batch, s.L, s.Hq, s.Hkv, s.D), dtype=torch.uint8,
+                     device=prep[0][0].device)
 
     def call(i):
         q, k, v, o_, do, lse, dq, dk, dv = prep[i % len(prep)]

@@ -42,7 +42,7 @@ _SIGNATURES = {
     "mars_version": (_I, []),
     "mars_last_cuda_error": (ctypes.c_char_p, []),
     "mars_train_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
-    "mars_train_attn_bwd_workspace_size": (_SZ, [_I, _I, _I]),
+    "mars_train_attn_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "mars_train_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_decode_attn_deferred": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
@@ -162,6 +162,10 @@ def train_attn(q, k, v, L: int, B: int, scale: float | None = None, o=None, lse=
     return (o, lse) if lse is not None else o
 
 
+def train_attn_bwd_workspace_size(batch: int, L: int, Hq: int, Hkv: int, D: int) -> int:
+    return int(_fn("mars_train_attn_bwd_workspace_size")(batch, L, Hq, Hkv, D))
+
+
 def train_attn_bwd(q, k, v, o, dout, lse, L: int, B: int, scale: float | None = None, dq=None, dk=None, dv=None,
                    workspace=None, status=None, stream=None):
     """Gradients of train_attn (include/mars.h: mars_train_attn_bwd).
@@ -186,7 +190,7 @@ def train_attn_bwd(q, k, v, o, dout, lse, L: int, B: int, scale: float | None = 
     _check(dk, "dk", torch.bfloat16, k.shape, dev)
     _check(dv, "dv", torch.bfloat16, v.shape, dev)
     if workspace is None:
-        n = int(_fn("mars_train_attn_bwd_workspace_size")(nb, L, hq))
+        n = int(_fn("mars_train_attn_bwd_workspace_size")(nb, L, hq, hkv, d))
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
     if status is not None:
         _check(status, "status", torch.int32, (1,), dev)

@@ -11,14 +11,17 @@
 //
 // sm_103a design (tensor-bound).  Three launches, no atomics, deterministic:
 //   1. delta_kernel: delta_i = rowsum(dO_i * O_i), fp32, one warp per row.
-//   2. bwd_kernel<kDKV>: one CTA per (sequence, KV head, 128-key tile).  For
-//      every query head of the group and every 128-row query tile that sees
-//      the key tile (an exact interval test on Eq. 2's structure), tcgen05
+//   2. bwd_kernel<kDKV>: one CTA per (sequence, query head, 128-key tile).  For
+//      every 128-row query tile that sees the key tile (an exact interval test
+//      on Eq. 2's structure), tcgen05
 //      computes S = Q K^T and dP = dO V^T into tensor memory; four warps (one
 //      query row per thread) form P and dS and write them to shared memory as
 //      SW128 [128 rows x 64 keys] tiles; tcgen05 then accumulates dV += P^T dO
 //      and dK += dS^T Q in tensor memory (the P / dS tiles are read MN-major
-//      as the A operand, Q / dO MN-major as B).
+//      as the A operand, Q / dO MN-major as B).  With GQA each query head's
+//      dK, dV go to an fp32 partial in the workspace and reduce_kernel sums the
+//      heads of a group in a fixed order (one unit per head keeps the heaviest
+//      key tile from serialising the whole group's work in one CTA).
 //   3. bwd_kernel<kDQ>: one CTA per (sequence, query head, 128-row query tile):
 //      the same S, dP, dS steps for every key tile the query tile sees, then
 //      dQ += dS K (dS K-major, K MN-major).
@@ -68,6 +71,7 @@ struct UnitOrder {
 struct BwdArgs {
   const float* lse;    // [b, Hq, 2L] natural log
   const float* delta;  // [b, Hq, 2L]
+  float* part;         // GQA: per-query-head fp32 dK | dV partials [2][b, 2L, Hq, D]; nullptr when G == 1
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
@@ -136,6 +140,35 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__
   if (lane == 0) delta[(static_cast<size_t>(b) * Hq + h) * n2 + i] = acc;
 }
 
+// ---------------------------------------------------------------- GQA reduction
+// dK (m = 0) and dV (m = 1) of KV head g: the sum over its G query heads' fp32
+// partials, in head order, rounded once to bf16.  Thread = 8 consecutive elements.
+__global__ void __launch_bounds__(256) reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ dk,
+                                                     uint16_t* __restrict__ dv, int batch, int n2, int Hkv, int G,
+                                                     int D) {
+  const long long e8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long per_m = static_cast<long long>(batch) * n2 * Hkv * D / 8;
+  if (e8 >= 2 * per_m) return;
+  const int m = static_cast<int>(e8 / per_m);
+  const long long r = e8 % per_m;
+  const int dc = static_cast<int>(r % (D / 8));
+  const long long rg = r / (D / 8);  // (b, i, g)
+  const int g = static_cast<int>(rg % Hkv);
+  const long long bi = rg / Hkv;
+  const int Hq = Hkv * G;
+  const float* src = part + ((static_cast<size_t>(m) * batch * n2 + bi) * Hq + static_cast<size_t>(g) * G) * D + 8 * dc;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int h = 0; h < G; ++h) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(h) * D));
+    const float4 y = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(h) * D + 4));
+    acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+    acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+  }
+  uint16_t* dst = (m == 0 ? dk : dv) + (rg * D + 8 * dc);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                              pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
 // ---------------------------------------------------------------- main kernel
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -151,17 +184,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- the unit: (b, g, key tile) for dKV, (b, h, query tile) for dQ; heaviest tiles first
   const int ntiles = 2 * a.nt;
-  const int heads = MODE == kDKV ? a.Hkv : a.Hq;
+  const int heads = a.Hq;  // one unit per query head in both modes
   const int per_tile = a.batch * heads;
   const int tile = order.tile[blockIdx.x / per_tile];
   const int rest = blockIdx.x % per_tile;
-  const int b = rest / heads, hh = rest % heads;  // hh: KV head (dKV) or query head (dQ)
+  const int b = rest / heads, hh = rest % heads;  // hh: the query head
   int u0, uend;
   tile_rows(a, tile, u0, uend);
   // The steps of the unit: every (query head of the group, query tile) that sees the
   // key tile (dKV), or every key tile the query tile sees (dQ), in index order.  Each
   // role walks them with its own iterator.
-  const int nsteps_heads = MODE == kDKV ? a.G : 1;
+  const int nsteps_heads = 1;
   struct Steps {
     int hs = 0, t = -1;
   };
@@ -173,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (MODE == kDKV ? tile_visible(a, it.t, tile) : tile_visible(a, tile, it.t)) break;
     }
-    head = MODE == kDKV ? hh * a.G + it.hs : hh;
+    head = hh;
     other = it.t;
   };
   int nsteps = 0;
@@ -200,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t ring_s = smem_u32(smem + C::RING_OFF);
   const uint32_t p_s = smem_u32(smem + C::P_OFF);
   const uint32_t ds_s = smem_u32(smem + C::DS_OFF);
-  const int g = MODE == kDKV ? hh : hh / a.G;  // KV head
+  const int g = hh / a.G;  // KV head
   bool ok = true;
 
   if (warp == 0) {
@@ -389,12 +422,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row = u0 + r;
       const bool store = row < uend;
+      const size_t srow = static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0);
 #pragma unroll 1
       for (int m = 0; m < (MODE == kDKV ? 2 : 1); ++m) {
+        const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
+        if (MODE == kDKV && a.part != nullptr) {
+          // fp32 partial of this query head, summed over the group by reduce_kernel
+          float4* out = reinterpret_cast<float4*>(a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + srow) *
+                                                                a.Hq + hh) * D);
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
+            tc_wait_ld();
+            if (store) {
+#pragma unroll
+              for (int w = 0; w < 8; ++w)
+                out[(c >> 2) + w] = nsteps > 0 ? make_float4(__uint_as_float(v[4 * w]) * f, __uint_as_float(v[4 * w + 1]) * f,
+                                                             __uint_as_float(v[4 * w + 2]) * f, __uint_as_float(v[4 * w + 3]) * f)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          continue;
+        }
         uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
         const int H = MODE == kDKV ? a.Hkv : a.Hq;
-        const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
-        uint4* out = reinterpret_cast<uint4*>(dst + ((static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0)) * H + hh) * D);
+        const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
+        uint4* out = reinterpret_cast<uint4*>(dst + (srow * H + hout) * D);
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t v[32];
@@ -478,7 +532,7 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
   }
   UnitOrder order;
   make_order(a, MODE, &order);
-  const long long units = 2LL * a.nt * a.batch * (MODE == kDKV ? a.Hkv : a.Hq);
+  const long long units = 2LL * a.nt * a.batch * a.Hq;
   bwd_kernel<D, MODE><<<static_cast<int>(units), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a, order);
   return mars_host::launch_status();
 }
@@ -487,9 +541,15 @@ inline size_t align_up(size_t x, size_t al) { return (x + al - 1) / al * al; }
 
 }  // namespace
 
-extern "C" size_t mars_train_attn_bwd_workspace_size(int batch, int L, int Hq) {
-  if (batch <= 0 || L <= 0 || Hq <= 0) return 0;
+// Workspace: delta [b, Hq, 2L] fp32, then (GQA only) the dK | dV partials [2][b, 2L, Hq, D] fp32.
+inline size_t delta_bytes(int batch, int L, int Hq) {
   return align_up(static_cast<size_t>(batch) * Hq * 2 * L * sizeof(float), 256);
+}
+
+extern "C" size_t mars_train_attn_bwd_workspace_size(int batch, int L, int Hq, int Hkv, int D) {
+  if (batch <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+  const size_t part = Hq == Hkv ? 0 : 2 * static_cast<size_t>(batch) * 2 * L * Hq * D * sizeof(float);
+  return delta_bytes(batch, L, Hq) + part;
 }
 
 extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o,
@@ -508,13 +568,16 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
   MARS_HOST_CHECK(lse != nullptr && mars_host::aligned4(lse), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(status == nullptr || mars_host::aligned4(status), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(workspace != nullptr && aligned16(workspace), MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(workspace_bytes >= mars_train_attn_bwd_workspace_size(batch, L, Hq), MARS_ERR_WORKSPACE_TOO_SMALL);
+  MARS_HOST_CHECK(workspace_bytes >= mars_train_attn_bwd_workspace_size(batch, L, Hq, Hkv, D),
+                  MARS_ERR_WORKSPACE_TOO_SMALL);
   int rc = mars_host::check_device();
   if (rc != MARS_OK) return rc;
 
   BwdArgs a;
   a.lse = lse;
   a.delta = static_cast<const float*>(workspace);
+  a.part = Hq == Hkv ? nullptr
+                     : reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(batch, L, Hq));
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
@@ -540,5 +603,11 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
   if (rc != MARS_OK) return rc;
   rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, s);
   if (rc != MARS_OK) return rc;
+  if (a.part != nullptr) {
+    const long long e8 = 2LL * batch * 2 * L * Hkv * D / 8;
+    reduce_kernel<<<static_cast<int>((e8 + 255) / 256), 256, 0, s>>>(a.part, dk, dv, batch, 2 * L, Hkv, a.G, D);
+    rc = mars_host::launch_status();
+    if (rc != MARS_OK) return rc;
+  }
   return D == 64 ? launch<64, kDQ>(tq, tk, tv, tdo, a, s) : launch<128, kDQ>(tq, tk, tv, tdo, a, s);
 }
