@@ -10,13 +10,13 @@
 // and P is recomputed from the forward's log-sum-exp: P = exp(S - lse).
 //
 // sm_103a design (tensor-bound).  Three launches, no atomics, deterministic:
-//   1. delta_kernel: delta_i = rowsum(dO_i * O_i), fp32, one warp per row.
+//   1. delta_kernel: delta_i = rowsum(dO_i * O_i), fp32, 16-byte loads.
 //   2. bwd_kernel<kDKV>: one CTA per (sequence, query head, 128-key tile).  For
 //      every 128-row query tile that sees the key tile (an exact interval test
 //      on Eq. 2's structure), tcgen05
-//      computes S = Q K^T and dP = dO V^T into tensor memory; four warps (one
-//      query row per thread) form P and dS and write them to shared memory as
-//      SW128 [128 rows x 64 keys] tiles; tcgen05 then accumulates dV += P^T dO
+//      computes S = Q K^T and dP = dO V^T into tensor memory; two warpgroups
+//      (one query row per thread, one 64-key half of the tile each) form P and
+//      dS and write them to shared memory as SW128 [128 rows x 64 keys] tiles; tcgen05 then accumulates dV += P^T dO
 //      and dK += dS^T Q in tensor memory (the P / dS tiles are read MN-major
 //      as the A operand, Q / dO MN-major as B).  With GQA each query head's
 //      dK, dV go to an fp32 partial in the workspace and reduce_kernel sums the
@@ -26,7 +26,9 @@
 //      the same S, dP, dS steps for every key tile the query tile sees, then
 //      dQ += dS K (dS K-major, K MN-major).
 // Roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one elected lane),
-// warps 2..5 elementwise (thread = TMEM lane = query row).  Every mbarrier wait
+// warps 2..5 and 6..9 elementwise (thread = TMEM lane = query row; warpgroup e
+// takes keys [64 e, 64 e + 64) of each step: P and dS need only per-row
+// constants, so the halves exchange nothing).  Every mbarrier wait
 // is bounded; a wait that gives up sets MARS_DEV_TIMEOUT.
 #include <cuda.h>
 
@@ -42,10 +44,17 @@ using namespace mars;
 
 constexpr int kT = 128;            // query rows of a query tile = keys of a key tile
 constexpr int kBox = 128 * 128;    // bytes of one [128 rows x 64 bf16] SW128 box
-constexpr int kThreads = 192;      // producer, MMA issuer, 4 elementwise warps
+constexpr int kThreads = 320;      // producer, MMA issuer, 2 x 4 elementwise warps
 constexpr int kMaxTiles = 1024;    // tiles per batch entry and head (2 * ceil(L / 128))
 
 enum Mode { kDKV = 0, kDQ = 1 };
+// (d0, d1) = (dp0 - t, dp1 - t) * (p0, p1) with packed fp32x2 arithmetic.
+__device__ __forceinline__ void sub_mul2(float dp0, float dp1, float t, float p0, float p1, float& d0, float& d1) {
+  asm("{\n .reg .b64 x, c, p, r;\n mov.b64 x, {%2, %3};\n mov.b64 c, {%4, %4};\n mov.b64 p, {%5, %6};\n"
+      " sub.rn.f32x2 r, x, c;\n mul.rn.f32x2 r, r, p;\n mov.b64 {%0, %1}, r;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(dp0), "f"(dp1), "f"(t), "f"(p0), "f"(p1));
+}
 
 template <int D, int MODE>
 struct BCfg {
@@ -119,25 +128,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 }
 
 // ---------------------------------------------------------------- delta
+// delta_i = sum_d dO_i O_i in fp32.  A row of D bf16 is D / 8 threads, each
+// reading one 16-byte chunk of O and of dO; the chunk sums meet by shuffles
+// inside the row's lanes (D / 8 divides 32).
 __global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                                     float* __restrict__ delta, int batch, int n2, int Hq, int D) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (b, i, h)
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(batch) * n2 * Hq) return;
-  const int h = static_cast<int>(row % Hq);
-  const long long bi = row / Hq;
-  const int i = static_cast<int>(bi % n2), b = static_cast<int>(bi / n2);
-  const uint16_t* po = o + row * D;
-  const uint16_t* pd = dout + row * D;
+  const int per_row = D / 8;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = tid / per_row;  // (b, i, h)
+  const int c = static_cast<int>(tid % per_row);
+  const bool valid = row < static_cast<long long>(batch) * n2 * Hq;
   float acc = 0.f;
-  for (int c = 2 * lane; c < D; c += 64) {
-    const uint32_t wo = *reinterpret_cast<const uint32_t*>(po + c), wd = *reinterpret_cast<const uint32_t*>(pd + c);
-    acc = fmaf(bf16lo_to_f32(wo), bf16lo_to_f32(wd), acc);
-    acc = fmaf(bf16hi_to_f32(wo), bf16hi_to_f32(wd), acc);
-  }
+  if (valid) {
+    const uint4 wo = __ldg(reinterpret_cast<const uint4*>(o + row * D) + c);
+    const uint4 wd = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + c);
+    const uint32_t po[4] = {wo.x, wo.y, wo.z, wo.w}, pd[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) delta[(static_cast<size_t>(b) * Hq + h) * n2 + i] = acc;
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(bf16lo_to_f32(po[e]), bf16lo_to_f32(pd[e]), acc);
+      acc = fmaf(bf16hi_to_f32(po[e]), bf16hi_to_f32(pd[e]), acc);
+    }
+  }
+  for (int s = per_row / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (valid && c == 0) {
+    const int h = static_cast<int>(row % Hq);
+    const long long bi = row / Hq;
+    const int i = static_cast<int>(bi % n2), b = static_cast<int>(bi / n2);
+    delta[(static_cast<size_t>(b) * Hq + h) * n2 + i] = acc;
+  }
 }
 
 // ---------------------------------------------------------------- GQA reduction
@@ -220,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_free[s], 1);
     }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, 128);
+    mbar_init(&bar_p, 256);
     mbar_init(&bar_acc, 1);
     fence_mbar_init();
   }
@@ -345,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================= elementwise: thread = TMEM lane = row of S (a query row)
+    const int ew = (warp - 2) >> 2;  // warpgroup: keys [64 ew, 64 ew + 64) of the tile
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
@@ -378,32 +397,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // (S(n) complete implies every earlier MMA is complete: the P / dS tiles are free)
-#pragma unroll 1
-      for (int hb = 0; hb < 2; ++hb) {  // keys [64 hb, 64 hb + 64): one SW128 box
+      {
+        const int hb = ew;  // keys [64 hb, 64 hb + 64): one SW128 box
         uint32_t sv[64], dpv[64];
         tmem_ld32(tmem + lane_addr + C::S_COL + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
         tmem_ld32(tmem + lane_addr + C::S_COL + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
         tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+        // The row's visible keys in this half as local columns [vlo, vhi] (empty when
+        // vlo > vhi): a key tile lies in one stream, so one interval of Eq. 2 applies.
+        const int kb = k0 + 64 * hb;
+        const bool clean_keys = k0 < a.L;
+        const int vlo = (clean_keys ? 0 : n_lo) - kb;
+        const int vhi = min(clean_keys ? c_hi : n_hi, ke - 1) - kb;
+        const bool full = __all_sync(0xffffffffu, vlo <= 0 && vhi >= 63);  // interior: no mask
         tc_wait_ld();
+        if (!full) {  // hidden scores become -inf: exp2 of them is exactly 0, and so is dS
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = (c >= vlo && c <= vhi) ? sv[c] : 0xFF800000u;
+        }
         const uint32_t row_off = static_cast<uint32_t>(hb * kBox + r * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // 8 keys = one 16-byte chunk
           uint32_t pw[4], dw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float pp[2], dd[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int c = 8 * q + 2 * e + u;
-              const int j = k0 + 64 * hb + c;
-              const bool vis = j < ke && (j <= c_hi || (j >= n_lo && j <= n_hi));
-              const float p = vis ? fast_exp2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -lse2)) : 0.f;
-              pp[u] = p;
-              dd[u] = p * (__uint_as_float(dpv[c]) - dlt);
-            }
-            pw[e] = pack_bf16x2(pp[0], pp[1]);
-            dw[e] = pack_bf16x2(dd[0], dd[1]);
+            const int c = 8 * q + 2 * e;
+            float x0, x1, d0, d1;
+            fma2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), a.scale_log2, -lse2, x0, x1);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            sub_mul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, p0, p1, d0, d1);
+            pw[e] = pack_bf16x2(p0, p1);
+            dw[e] = pack_bf16x2(d0, d1);
           }
           const uint32_t sw = static_cast<uint32_t>(((q ^ (r & 7)) * 16));
           if (MODE == kDKV) st_shared_v4(p_s + row_off + sw, pw[0], pw[1], pw[2], pw[3]);
@@ -423,15 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = u0 + r;
       const bool store = row < uend;
       const size_t srow = static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0);
-#pragma unroll 1
-      for (int m = 0; m < (MODE == kDKV ? 2 : 1); ++m) {
+      // warpgroup ew writes dK (ew = 0) or dV (ew = 1) in dKV mode, and columns
+      // [D/2 ew, D/2 (ew + 1)) of dQ in dQ mode
+      const int c_lo = MODE == kDKV ? 0 : (D / 2) * ew, c_hi = MODE == kDKV ? D : (D / 2) * (ew + 1);
+      {
+        const int m = MODE == kDKV ? ew : 0;
         const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
         if (MODE == kDKV && a.part != nullptr) {
           // fp32 partial of this query head, summed over the group by reduce_kernel
           float4* out = reinterpret_cast<float4*>(a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + srow) *
                                                                 a.Hq + hh) * D);
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
+          for (int c = c_lo; c < c_hi; c += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
             tc_wait_ld();
@@ -443,24 +471,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                : make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
-          continue;
-        }
-        uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
-        const int H = MODE == kDKV ? a.Hkv : a.Hq;
-        const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
-        uint4* out = reinterpret_cast<uint4*>(dst + (srow * H + hout) * D);
+        } else {
+          uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
+          const int H = MODE == kDKV ? a.Hkv : a.Hq;
+          const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
+          uint4* out = reinterpret_cast<uint4*>(dst + (srow * H + hout) * D);
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
-          tc_wait_ld();
-          uint32_t pk[16];
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
+            tc_wait_ld();
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f) : 0u;
-          if (store) {
+            for (int e = 0; e < 16; ++e)
+              pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f) : 0u;
+            if (store) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) out[(c >> 3) + w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+              for (int w = 0; w < 4; ++w) out[(c >> 3) + w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+            }
           }
         }
       }
@@ -597,8 +625,8 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
     return MARS_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
-  delta_kernel<<<static_cast<int>((rows + 7) / 8), 256, 0, s>>>(o, dout, static_cast<float*>(workspace), batch, 2 * L,
-                                                               Hq, D);
+  delta_kernel<<<static_cast<int>((rows * (D / 8) + 255) / 256), 256, 0, s>>>(o, dout, static_cast<float*>(workspace),
+                                                                              batch, 2 * L, Hq, D);
   rc = mars_host::launch_status();
   if (rc != MARS_OK) return rc;
   rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, s);
