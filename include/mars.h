@@ -104,12 +104,15 @@ int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  *   k, v       [batch, 2L, Hkv, D] bf16       dk, dv [batch, 2L, Hkv, D] bf16 (written)
  *   lse        [batch, Hq, 2L] fp32 (the forward's, natural log)
  *   workspace  device buffer of >= mars_train_attn_bwd_workspace_size(batch,
- *              L, Hq, Hkv, D) bytes (it holds rowsum(dO * o) and, when Hq > Hkv,
- *              each query head's fp32 dK, dV before the group sum); contents on
- *              entry do not matter; calls that share it must not overlap in time.
+ *              L, Hq, Hkv, D) bytes (it holds rowsum(dO * o), two work counters
+ *              and, when Hq > Hkv, each query head's fp32 dK, dV before the group
+ *              sum); contents on entry do not matter; calls that share it must
+ *              not overlap in time.
  * Kernel launches on `stream`: the row sums, dK and dV per (query head, key
- * tile), the sum over each GQA group (when Hq > Hkv), then dQ per query tile;
- * no atomics, so the result is deterministic.  Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= B;
+ * tile), the sum over each GQA group (when Hq > Hkv), then dQ per query tile.
+ * Persistent CTAs take work units from an atomic counter, but every output
+ * element comes from one fixed sequence of operations whichever CTA runs it, so
+ * the result is deterministic.  Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= B;
  * 1 <= L <= 65536.  All pointers 16-byte aligned except lse (4 bytes).
  */
 size_t mars_train_attn_bwd_workspace_size(int batch, int L, int Hq, int Hkv, int D);

@@ -9,27 +9,31 @@
 //   dQ = scale dS k,  dK = scale dS^T q,
 // and P is recomputed from the forward's log-sum-exp: P = exp(S - lse).
 //
-// sm_103a design (tensor-bound).  Three launches, no atomics, deterministic:
+// sm_103a design (tensor-bound).  Three launches, deterministic (the only atomic
+// hands out work units):
 //   1. delta_kernel: delta_i = rowsum(dO_i * O_i), fp32, 16-byte loads.
-//   2. bwd_kernel<kDKV>: one CTA per (sequence, query head, 128-key tile).  For
+//   2. bwd_kernel<kDKV>: one unit per (sequence, query head, 128-key tile).  For
 //      every 128-row query tile that sees the key tile (an exact interval test
-//      on Eq. 2's structure), tcgen05
-//      computes S = Q K^T and dP = dO V^T into tensor memory; two warpgroups
-//      (one query row per thread, one 64-key half of the tile each) form P and
-//      dS and write them to shared memory as SW128 [128 rows x 64 keys] tiles; tcgen05 then accumulates dV += P^T dO
-//      and dK += dS^T Q in tensor memory (the P / dS tiles are read MN-major
-//      as the A operand, Q / dO MN-major as B).  With GQA each query head's
-//      dK, dV go to an fp32 partial in the workspace and reduce_kernel sums the
-//      heads of a group in a fixed order (one unit per head keeps the heaviest
-//      key tile from serialising the whole group's work in one CTA).
-//   3. bwd_kernel<kDQ>: one CTA per (sequence, query head, 128-row query tile):
-//      the same S, dP, dS steps for every key tile the query tile sees, then
+//      on Eq. 2's structure) tcgen05 computes dP = dO V^T and S = Q K^T into
+//      tensor memory; the elementwise warps form P and dS and write them to
+//      shared memory as SW128 [128 rows x 64 keys] tiles; tcgen05 then
+//      accumulates dV += P^T dO and dK += dS^T Q in tensor memory (P / dS read
+//      MN-major as the A operand, Q / dO MN-major as B).  With GQA each query
+//      head's dK, dV go to an fp32 partial in the workspace and reduce_kernel
+//      sums the heads of a group in a fixed order (one unit per head keeps the
+//      heaviest key tile from serialising a whole group's work).
+//   3. bwd_kernel<kDQ>: one unit per (sequence, query head, 128-row query tile):
+//      the same dP, S, dS for every key tile the query tile sees, then
 //      dQ += dS K (dS K-major, K MN-major).
-// Roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one elected lane),
-// warps 2..5 and 6..9 elementwise (thread = TMEM lane = query row; warpgroup e
-// takes keys [64 e, 64 e + 64) of each step: P and dS need only per-row
-// constants, so the halves exchange nothing).  Every mbarrier wait
-// is bounded; a wait that gives up sets MARS_DEV_TIMEOUT.
+// CTAs are persistent (one per SM) and take units heaviest first from a work
+// counter.  Roles: warp 0 TMA producer (the unit's fixed tiles, then a ring of
+// single-tile slots with the per-step tiles, each slot freed by the commit after
+// its last reader), warp 1 MMA issuer (one elected lane), warps 2..5 and 6..9
+// elementwise (thread = TMEM lane = query row; warpgroup e takes keys
+// [64 e, 64 e + 64): P and dS need only per-row constants, so the halves
+// exchange nothing).  The elementwise warps release S, dP as soon as they hold
+// them in registers, so the next step's products overlap their work.  Every
+// mbarrier wait is bounded; a wait that gives up sets MARS_DEV_TIMEOUT.
 #include <cuda.h>
 
 #include <algorithm>
@@ -44,7 +48,9 @@ using namespace mars;
 
 constexpr int kT = 128;            // query rows of a query tile = keys of a key tile
 constexpr int kBox = 128 * 128;    // bytes of one [128 rows x 64 bf16] SW128 box
-constexpr int kThreads = 320;      // producer, MMA issuer, 2 x 4 elementwise warps
+constexpr int kEW = 2;             // elementwise warpgroups, each 128 / kEW keys of a step
+constexpr int kEWCols = kT / kEW;
+constexpr int kThreads = 64 + 128 * kEW;  // producer, MMA issuer, elementwise warps
 constexpr int kMaxTiles = 1024;    // tiles per batch entry and head (2 * ceil(L / 128))
 
 enum Mode { kDKV = 0, kDQ = 1 };
@@ -60,12 +66,18 @@ template <int D, int MODE>
 struct BCfg {
   static constexpr int NB = D / 64;
   static constexpr int TILE = NB * kBox;  // one [128 x D] bf16 tile
-  // dKV: the unit's K and V once, Q and dO in NS stages.  dQ: the unit's Q and
-  // dO once, K and V in NS stages.  Both: P (dKV only) and dS [128 x 128] tiles.
-  static constexpr int NS = (MODE == kDKV && D == 128) ? 1 : 2;  // 256 KB would not fit at D = 128
+  // dKV: the unit's K and V once; a ring of single-tile slots takes dO(n), Q(n),
+  // dO(n + 1), ... in that order.  dQ: the unit's Q and dO once; the ring takes
+  // V(n), K(n), V(n + 1), ...  Both: P (dKV only) and dS [128 x 128] tiles.  A
+  // slot is released by the commit after the last product that reads it, so the
+  // next step's tiles load while this step's products run.
+  static constexpr int NSLOT = (MODE == kDKV && D == 128) ? 3 : 4;  // 3: 225 KB of 227 at D = 128
+  // S(n + 1) ahead of step n's accumulating products needs both tiles of steps n
+  // and n + 1 resident: four slots.  With three, only dP(n + 1) goes ahead.
+  static constexpr bool EARLY_S = NSLOT >= 4;
   static constexpr int FIXED_OFF = 0;                   // K, V (dKV) or Q, dO (dQ)
-  static constexpr int RING_OFF = FIXED_OFF + 2 * TILE;  // stage s: Q, dO (dKV) or K, V (dQ)
-  static constexpr int P_OFF = RING_OFF + NS * 2 * TILE;
+  static constexpr int RING_OFF = FIXED_OFF + 2 * TILE;
+  static constexpr int P_OFF = RING_OFF + NSLOT * TILE;
   static constexpr int DS_OFF = P_OFF + (MODE == kDKV ? 2 * kBox : 0);
   static constexpr int SMEM = DS_OFF + 2 * kBox + 1024;  // + slack to align the base to 1024
   static constexpr int S_COL = 0, DP_COL = kT, ACC_COL = 2 * kT;  // ACC: dK | dV, or dQ
@@ -81,6 +93,7 @@ struct BwdArgs {
   const float* lse;    // [b, Hq, 2L] natural log
   const float* delta;  // [b, Hq, 2L]
   float* part;         // GQA: per-query-head fp32 dK | dV partials [2][b, 2L, Hq, D]; nullptr when G == 1
+  int* next_unit;      // work counter of the launch (zeroed by delta_kernel)
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
@@ -132,7 +145,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 // reading one 16-byte chunk of O and of dO; the chunk sums meet by shuffles
 // inside the row's lanes (D / 8 divides 32).
 __global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                    float* __restrict__ delta, int batch, int n2, int Hq, int D) {
+                                                    float* __restrict__ delta, int* __restrict__ counters, int batch,
+                                                    int n2, int Hq, int D) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) counters[threadIdx.x] = 0;  // the two work counters of bwd_kernel
   const int per_row = D / 8;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = tid / per_row;  // (b, i, h)
@@ -196,50 +211,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = BCfg<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_fixed, bar_stage[C::NS], bar_free[C::NS], bar_s, bar_p, bar_acc;
+  __shared__ __align__(8) uint64_t bar_fixed, bar_ffree, bar_stage[C::NSLOT], bar_free[C::NSLOT], bar_s, bar_sdp, bar_p, bar_pfree,
+      bar_acc;
   __shared__ uint32_t tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- the unit: (b, g, key tile) for dKV, (b, h, query tile) for dQ; heaviest tiles first
+  // ---- units: (b, query head, key tile) for dKV, (b, query head, query tile) for
+  // dQ, listed heaviest tile first.  The CTAs are persistent: each takes its first
+  // unit by its index and every further one from the launch's work counter, so
+  // the heavy units spread over the SMs and the light ones fill in behind them.
+  // The producer fetches; it publishes the r-th unit of the CTA in queue slot
+  // r % 4 (bar_unit[r % 4]) for the other roles.  It runs at most three units
+  // ahead of the elementwise warps (it fetches unit r + 2 only after unit r's last
+  // S, which comes after the elementwise warps' P of unit r - 1), so four slots
+  // suffice.
   const int ntiles = 2 * a.nt;
-  const int heads = a.Hq;  // one unit per query head in both modes
-  const int per_tile = a.batch * heads;
-  const int tile = order.tile[blockIdx.x / per_tile];
-  const int rest = blockIdx.x % per_tile;
-  const int b = rest / heads, hh = rest % heads;  // hh: the query head
-  int u0, uend;
-  tile_rows(a, tile, u0, uend);
-  // The steps of the unit: every (query head of the group, query tile) that sees the
-  // key tile (dKV), or every key tile the query tile sees (dQ), in index order.  Each
-  // role walks them with its own iterator.
-  const int nsteps_heads = 1;
-  struct Steps {
-    int hs = 0, t = -1;
+  const int per_tile = a.batch * a.Hq;
+  const int nunits = ntiles * per_tile;
+  struct Unit {
+    int tile, b, hh, g, u0, uend, nsteps;
   };
-  auto next_step = [&](Steps& it, int& head, int& other) {
-    while (true) {
-      if (++it.t == ntiles) {
-        it.t = 0;
-        if (++it.hs == nsteps_heads) return;
-      }
-      if (MODE == kDKV ? tile_visible(a, it.t, tile) : tile_visible(a, tile, it.t)) break;
+  __shared__ int unit_q[4];
+  __shared__ __align__(8) uint64_t bar_unit[4];
+  auto unit_of = [&](int u, Unit& U) {
+    U.tile = order.tile[u / per_tile];
+    const int rest = static_cast<int>(u % per_tile);
+    U.b = rest / a.Hq;
+    U.hh = rest % a.Hq;  // the query head
+    U.g = U.hh / a.G;    // its KV head
+    tile_rows(a, U.tile, U.u0, U.uend);
+    U.nsteps = 0;
+    for (int o = 0; o < ntiles; ++o) U.nsteps += MODE == kDKV ? tile_visible(a, o, U.tile) : tile_visible(a, U.tile, o);
+  };
+  // the r-th unit of this CTA as the consumers see it: false at the end (or on a timeout)
+  auto unit = [&](int r, Unit& U) -> bool {
+    if (!mbar_wait(&bar_unit[r & 3], (r >> 2) & 1)) {
+      set_status(a.status, MARS_DEV_TIMEOUT);
+      return false;
     }
-    head = hh;
-    other = it.t;
+    const int u = unit_q[r & 3];
+    if (u < 0) return false;
+    unit_of(u, U);
+    return true;
   };
-  int nsteps = 0;
-  for (int t = 0; t < ntiles; ++t) nsteps += (MODE == kDKV ? tile_visible(a, t, tile) : tile_visible(a, tile, t));
-  nsteps *= nsteps_heads;
+  // The steps of a unit: every query tile that sees its key tile (dKV), or every key
+  // tile its query tile sees (dQ), in index order; each role walks them itself.
+  auto next_other = [&](const Unit& U, int o) {  // the first such tile after o
+    while (++o < ntiles && !(MODE == kDKV ? tile_visible(a, o, U.tile) : tile_visible(a, U.tile, o))) {
+    }
+    return o;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_fixed, 1);
-    for (int s = 0; s < C::NS; ++s) {
+    mbar_init(&bar_ffree, 1);  // a unit's last S and dP have read the fixed tiles
+    for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(&bar_stage[s], 1);
       mbar_init(&bar_free[s], 1);
     }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, 256);
+    mbar_init(&bar_sdp, 128 * kEW);  // S(n), dP(n) are in the elementwise warps' registers
+    mbar_init(&bar_p, 128 * kEW);
+    mbar_init(&bar_pfree, 1);  // step n's accumulating products are complete
     mbar_init(&bar_acc, 1);
+    for (int s = 0; s < 4; ++s) mbar_init(&bar_unit[s], 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&tmem_slot, 512);
@@ -251,43 +286,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t ring_s = smem_u32(smem + C::RING_OFF);
   const uint32_t p_s = smem_u32(smem + C::P_OFF);
   const uint32_t ds_s = smem_u32(smem + C::DS_OFF);
-  const int g = hh / a.G;  // KV head
   bool ok = true;
 
   if (warp == 0) {
     // ================= TMA producer
     if (lane == 0) {
-      // fixed operands: K, V of the key tile (dKV) or Q, dO of the query tile (dQ)
-      mbar_arrive_expect_tx(&bar_fixed, 2 * C::TILE);
-      for (int c = 0; c < C::NB; ++c) {
-        if (MODE == kDKV) {
-          tma_load_4d(fixed_s + c * kBox, &tm_k, &bar_fixed, 64 * c, g, u0, b);
-          tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_v, &bar_fixed, 64 * c, g, u0, b);
-        } else {
-          tma_load_4d(fixed_s + c * kBox, &tm_q, &bar_fixed, 64 * c, hh, u0, b);
-          tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_do, &bar_fixed, 64 * c, hh, u0, b);
-        }
-      }
-      Steps sit;
-      for (int n = 0; n < nsteps; ++n) {
-        const int st = n % C::NS;
-        if (n >= C::NS && !mbar_wait(&bar_free[st], ((n / C::NS) - 1) & 1)) {
+      int gt = 0;  // ring tiles issued
+      Unit U;
+      for (int r = 0; ok; ++r) {
+        const int u = r == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(a.next_unit, 1);
+        unit_q[r & 3] = u < nunits ? u : -1;
+        mbar_arrive(&bar_unit[r & 3]);  // release: the slot is written
+        if (u >= nunits) break;
+        unit_of(u, U);
+        // fixed operands: K, V of the key tile (dKV) or Q, dO of the query tile (dQ),
+        // once the previous unit's last S and dP have read theirs
+        if (r > 0 && !mbar_wait(&bar_ffree, (r - 1) & 1)) {
           set_status(a.status, MARS_DEV_TIMEOUT);
           break;
         }
-        int head = 0, other = 0;
-        next_step(sit, head, other);
-        int o0, oe;
-        tile_rows(a, other, o0, oe);
-        const uint32_t dst = ring_s + st * 2 * C::TILE;
-        mbar_arrive_expect_tx(&bar_stage[st], 2 * C::TILE);
+        mbar_arrive_expect_tx(&bar_fixed, 2 * C::TILE);
         for (int c = 0; c < C::NB; ++c) {
           if (MODE == kDKV) {
-            tma_load_4d(dst + c * kBox, &tm_q, &bar_stage[st], 64 * c, head, o0, b);
-            tma_load_4d(dst + C::TILE + c * kBox, &tm_do, &bar_stage[st], 64 * c, head, o0, b);
+            tma_load_4d(fixed_s + c * kBox, &tm_k, &bar_fixed, 64 * c, U.g, U.u0, U.b);
+            tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_v, &bar_fixed, 64 * c, U.g, U.u0, U.b);
           } else {
-            tma_load_4d(dst + c * kBox, &tm_k, &bar_stage[st], 64 * c, g, o0, b);
-            tma_load_4d(dst + C::TILE + c * kBox, &tm_v, &bar_stage[st], 64 * c, g, o0, b);
+            tma_load_4d(fixed_s + c * kBox, &tm_q, &bar_fixed, 64 * c, U.hh, U.u0, U.b);
+            tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_do, &bar_fixed, 64 * c, U.hh, U.u0, U.b);
+          }
+        }
+        for (int n = 0, ot = -1; ok && n < U.nsteps; ++n) {
+          ot = next_other(U, ot);
+          int o0, oe;
+          tile_rows(a, ot, o0, oe);
+          for (int y = 0; y < 2; ++y) {  // ring tiles of a step: dO, Q (dKV) or V, K (dQ)
+            const int tt = gt++, sl = tt % C::NSLOT;
+            if (tt >= C::NSLOT && !mbar_wait(&bar_free[sl], ((tt / C::NSLOT) - 1) & 1)) {
+              set_status(a.status, MARS_DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+            const CUtensorMap* tm = MODE == kDKV ? (y ? &tm_q : &tm_do) : (y ? &tm_k : &tm_v);
+            const int hc = MODE == kDKV ? U.hh : U.g;
+            const uint32_t dst = ring_s + sl * C::TILE;
+            mbar_arrive_expect_tx(&bar_stage[sl], C::TILE);
+            for (int c = 0; c < C::NB; ++c) tma_load_4d(dst + c * kBox, tm, &bar_stage[sl], 64 * c, hc, o0, U.b);
           }
         }
       }
@@ -300,36 +343,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_acc = MODE == kDKV ? idesc_bf16(kT, D, true, true)   // P^T dO, dS^T Q
                                              : idesc_bf16(kT, D, false, true); // dS K
     auto wait_all = [&](uint64_t* bar, int parity) { ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
-    wait_all(&bar_fixed, 0);
-    tc_fence_after();
-    for (int n = 0; ok && n < nsteps; ++n) {
-      const int st = n % C::NS;
-      wait_all(&bar_stage[st], (n / C::NS) & 1);
-      if (!ok) break;
+    // Ring tiles of step n: x = 2n (dO or V) and y = 2n + 1 (Q or K); the fixed
+    // tiles are the others.
+    auto tiles = [&](int n, uint32_t& q_t, uint32_t& do_t, uint32_t& k_t, uint32_t& v_t) {
+      const uint32_t x_t = ring_s + ((2 * n) % C::NSLOT) * C::TILE, y_t = ring_s + ((2 * n + 1) % C::NSLOT) * C::TILE;
+      q_t = MODE == kDKV ? y_t : fixed_s;
+      do_t = MODE == kDKV ? x_t : fixed_s + C::TILE;
+      k_t = MODE == kDKV ? fixed_s : y_t;
+      v_t = MODE == kDKV ? fixed_s + C::TILE : x_t;
+    };
+    // dP(n) = dO V^T (its ring tile x is loaded first)
+    auto issue_dp = [&](int n) {
+      const int tx = 2 * n, sx = tx % C::NSLOT;
+      wait_all(&bar_stage[sx], (tx / C::NSLOT) & 1);
+      if (!ok) return;
       tc_fence_after();
-      const uint32_t stage = ring_s + st * 2 * C::TILE;
-      // Q and dO tiles: the fixed ones (dQ) or this step's (dKV); K and V the other way round
-      const uint32_t q_t = MODE == kDKV ? stage : fixed_s, do_t = q_t + C::TILE;
-      const uint32_t k_t = MODE == kDKV ? fixed_s : stage, v_t = k_t + C::TILE;
+      uint32_t q_t, do_t, k_t, v_t;
+      tiles(n, q_t, do_t, k_t, v_t);
       if (leader) {
-        const uint64_t dq_ = smem_desc(q_t, 16, 1024), dk_ = smem_desc(k_t, 16, 1024);
         const uint64_t ddo = smem_desc(do_t, 16, 1024), dv_ = smem_desc(v_t, 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
-          tc_mma_ss(tmem + C::S_COL, dq_ + off, dk_ + off, id_s, ks > 0 ? 1u : 0u);
-        }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
           tc_mma_ss(tmem + C::DP_COL, ddo + off, dv_ + off, id_s, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&bar_s);
+        if (MODE == kDQ) tc_commit(&bar_free[sx]);  // V(n) has no other reader
       }
       __syncwarp();
-      wait_all(&bar_p, n & 1);  // P and dS are in shared memory
-      if (!ok) break;
+    };
+    // S(n) = Q K^T, then "S(n) and dP(n) ready" (and, after a unit's last step,
+    // "the fixed tiles may be replaced")
+    auto issue_s = [&](int n, bool unit_last) {
+      const int ty = 2 * n + 1, sy = ty % C::NSLOT;
+      wait_all(&bar_stage[sy], (ty / C::NSLOT) & 1);
+      if (!ok) return;
       tc_fence_after();
+      uint32_t q_t, do_t, k_t, v_t;
+      tiles(n, q_t, do_t, k_t, v_t);
+      if (leader) {
+        const uint64_t dq_ = smem_desc(q_t, 16, 1024), dk_ = smem_desc(k_t, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
+          tc_mma_ss(tmem + C::S_COL, dq_ + off, dk_ + off, id_s, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&bar_s);
+        if (unit_last) tc_commit(&bar_ffree);
+      }
+      __syncwarp();
+    };
+    // the accumulating products of step n, once its P and dS are in shared memory;
+    // the first step of a unit starts the accumulators afresh
+    auto issue_acc = [&](int n, bool first, bool last) {
+      wait_all(&bar_p, n & 1);
+      if (!ok) return;
+      tc_fence_after();
+      const int sx = (2 * n) % C::NSLOT, sy = (2 * n + 1) % C::NSLOT;
+      uint32_t q_t, do_t, k_t, v_t;
+      tiles(n, q_t, do_t, k_t, v_t);
       if (leader) {
         if (MODE == kDKV) {
           // dV += P^T dO and dK += dS^T Q over the 128 query rows (16 per step)
@@ -338,12 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks) {
             const uint32_t off = (ks * 16 * 128) >> 4;
-            tc_mma_ss(tmem + C::ACC_COL + D, dpa + off, ddo + off, id_acc, (n > 0 || ks > 0) ? 1u : 0u);
+            tc_mma_ss(tmem + C::ACC_COL + D, dpa + off, ddo + off, id_acc, (!first || ks > 0) ? 1u : 0u);
           }
+          tc_commit(&bar_free[sx]);  // dO(n): read by dP and dV, both issued
 #pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks) {
             const uint32_t off = (ks * 16 * 128) >> 4;
-            tc_mma_ss(tmem + C::ACC_COL, dsa + off, dqb + off, id_acc, (n > 0 || ks > 0) ? 1u : 0u);
+            tc_mma_ss(tmem + C::ACC_COL, dsa + off, dqb + off, id_acc, (!first || ks > 0) ? 1u : 0u);
           }
         } else {
           // dQ += dS K over the 128 keys (16 per step): dS K-major, K MN-major
@@ -351,143 +423,193 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kT / 16; ++ks) {
             const uint32_t aoff = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4, boff = (ks * 16 * 128) >> 4;
-            tc_mma_ss(tmem + C::ACC_COL, dsa + aoff, dkb + boff, id_acc, (n > 0 || ks > 0) ? 1u : 0u);
+            tc_mma_ss(tmem + C::ACC_COL, dsa + aoff, dkb + boff, id_acc, (!first || ks > 0) ? 1u : 0u);
           }
         }
-        tc_commit(&bar_free[st]);
-        if (n + 1 == nsteps) tc_commit(&bar_acc);
+        tc_commit(&bar_free[sy]);  // Q(n) (read by S, dK) or K(n) (read by S, dQ)
+        tc_commit(&bar_pfree);     // the P / dS tiles may be overwritten
+        if (last) tc_commit(&bar_acc);
       }
       __syncwarp();
+    };
+    // Step n + 1's dP (and S, when the ring holds both of its tiles beside step
+    // n's) is issued as soon as the elementwise warps hold S(n), dP(n) in
+    // registers, so the tensor cores work while P(n), dS(n) are formed.  Steps are
+    // numbered over all the units of the CTA (gs); a unit's first dP and S may run
+    // while the elementwise warps write the previous unit's accumulators out.
+    int gs = 0;
+    Unit U;
+    for (int r = 0; ok && unit(r, U); ++r) {
+      wait_all(&bar_fixed, r & 1);
+      if (!ok) break;
+      tc_fence_after();
+      const int N = U.nsteps;
+      if (N == 0) {
+        if (leader) tc_commit(&bar_ffree);
+        __syncwarp();
+        continue;
+      }
+      issue_dp(gs);
+      issue_s(gs, N == 1);
+      for (int n = 0; ok && n < N; ++n, ++gs) {
+        const bool next = n + 1 < N;
+        if (next) {
+          wait_all(&bar_sdp, gs & 1);
+          issue_dp(gs + 1);
+          if (C::EARLY_S) issue_s(gs + 1, n + 2 == N);
+        }
+        issue_acc(gs, n == 0, n + 1 == N);
+        if (next && !C::EARLY_S) issue_s(gs + 1, n + 2 == N);
+      }
     }
     if (!ok && leader) set_status(a.status, MARS_DEV_TIMEOUT);
     __syncwarp();
   } else {
     // ================= elementwise: thread = TMEM lane = row of S (a query row)
-    const int ew = (warp - 2) >> 2;  // warpgroup: keys [64 ew, 64 ew + 64) of the tile
+    const int ew = (warp - 2) >> 2;  // warpgroup: keys [kEWCols ew, kEWCols (ew + 1)) of the tile
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    Steps sit;
-    for (int n = 0; n < nsteps; ++n) {
-      int head = 0, other = 0;
-      next_step(sit, head, other);
-      // query tile and key tile of this step
-      const int qt = MODE == kDKV ? other : tile, kt = MODE == kDKV ? tile : other;
-      int q0, qe, k0, ke;
-      tile_rows(a, qt, q0, qe);
-      tile_rows(a, kt, k0, ke);
-      const int i = q0 + r;
-      const bool row_ok = i < qe;
-      // visible keys of row i (Eq. 2): clean [0, c_hi], noisy [n_lo, n_hi]
-      int c_hi = -1, n_lo = 1, n_hi = 0;
-      if (row_ok) {
-        if (i < a.L) {
-          c_hi = i;
-        } else {
-          const int c = a.B * ((i - a.L) / a.B);
-          c_hi = c - 1;
-          n_lo = a.L + c;
-          n_hi = i;
-        }
-      }
-      const size_t ri = (static_cast<size_t>(b) * a.Hq + head) * (2 * a.L) + (row_ok ? i : 0);
-      const float lse2 = row_ok ? __ldg(a.lse + ri) * kLog2e : 0.f;
-      const float dlt = row_ok ? __ldg(a.delta + ri) : 0.f;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s, n & 1));
-      if (!ok) break;
-      tc_fence_after();
-      // (S(n) complete implies every earlier MMA is complete: the P / dS tiles are free)
-      {
-        const int hb = ew;  // keys [64 hb, 64 hb + 64): one SW128 box
-        uint32_t sv[64], dpv[64];
-        tmem_ld32(tmem + lane_addr + C::S_COL + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tmem + lane_addr + C::S_COL + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
-        tmem_ld32(tmem + lane_addr + C::DP_COL + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
-        // The row's visible keys in this half as local columns [vlo, vhi] (empty when
-        // vlo > vhi): a key tile lies in one stream, so one interval of Eq. 2 applies.
-        const int kb = k0 + 64 * hb;
-        const bool clean_keys = k0 < a.L;
-        const int vlo = (clean_keys ? 0 : n_lo) - kb;
-        const int vhi = min(clean_keys ? c_hi : n_hi, ke - 1) - kb;
-        const bool full = __all_sync(0xffffffffu, vlo <= 0 && vhi >= 63);  // interior: no mask
-        tc_wait_ld();
-        if (!full) {  // hidden scores become -inf: exp2 of them is exactly 0, and so is dS
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = (c >= vlo && c <= vhi) ? sv[c] : 0xFF800000u;
-        }
-        const uint32_t row_off = static_cast<uint32_t>(hb * kBox + r * 128);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {  // 8 keys = one 16-byte chunk
-          uint32_t pw[4], dw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * q + 2 * e;
-            float x0, x1, d0, d1;
-            fma2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), a.scale_log2, -lse2, x0, x1);
-            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            sub_mul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, p0, p1, d0, d1);
-            pw[e] = pack_bf16x2(p0, p1);
-            dw[e] = pack_bf16x2(d0, d1);
+    int gs = 0, nacc = 0;  // steps done (over all units), units whose accumulators were read
+    Unit U;
+    for (int ur = 0; ok && unit(ur, U); ++ur) {
+      const int b = U.b, hh = U.hh, g = U.g, tile = U.tile, u0 = U.u0, uend = U.uend, nsteps = U.nsteps;
+      for (int n = 0, ot = -1; n < nsteps; ++n, ++gs) {
+        ot = next_other(U, ot);
+        const int head = hh;
+        // query tile and key tile of this step
+        const int qt = MODE == kDKV ? ot : tile, kt = MODE == kDKV ? tile : ot;
+        int q0, qe, k0, ke;
+        tile_rows(a, qt, q0, qe);
+        tile_rows(a, kt, k0, ke);
+        const int i = q0 + r;
+        const bool row_ok = i < qe;
+        // visible keys of row i (Eq. 2): clean [0, c_hi], noisy [n_lo, n_hi]
+        int c_hi = -1, n_lo = 1, n_hi = 0;
+        if (row_ok) {
+          if (i < a.L) {
+            c_hi = i;
+          } else {
+            const int c = a.B * ((i - a.L) / a.B);
+            c_hi = c - 1;
+            n_lo = a.L + c;
+            n_hi = i;
           }
-          const uint32_t sw = static_cast<uint32_t>(((q ^ (r & 7)) * 16));
-          if (MODE == kDKV) st_shared_v4(p_s + row_off + sw, pw[0], pw[1], pw[2], pw[3]);
-          st_shared_v4(ds_s + row_off + sw, dw[0], dw[1], dw[2], dw[3]);
         }
-      }
-      fence_async_smem();  // the generic-proxy stores become visible to the tensor core
-      tc_fence_before();
-      mbar_arrive(&bar_p);
-    }
-    // ---- epilogue: the accumulators (rows = keys for dK, dV; query rows for dQ)
-    if (ok && nsteps > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc, 0));
-    if (!ok) {
-      if (lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
-    } else {
-      tc_fence_after();
-      const int row = u0 + r;
-      const bool store = row < uend;
-      const size_t srow = static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0);
-      // warpgroup ew writes dK (ew = 0) or dV (ew = 1) in dKV mode, and columns
-      // [D/2 ew, D/2 (ew + 1)) of dQ in dQ mode
-      const int c_lo = MODE == kDKV ? 0 : (D / 2) * ew, c_hi = MODE == kDKV ? D : (D / 2) * (ew + 1);
-      {
-        const int m = MODE == kDKV ? ew : 0;
-        const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
-        if (MODE == kDKV && a.part != nullptr) {
-          // fp32 partial of this query head, summed over the group by reduce_kernel
-          float4* out = reinterpret_cast<float4*>(a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + srow) *
-                                                                a.Hq + hh) * D);
-#pragma unroll 1
-          for (int c = c_lo; c < c_hi; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
-            tc_wait_ld();
-            if (store) {
+        const size_t ri = (static_cast<size_t>(b) * a.Hq + head) * (2 * a.L) + (row_ok ? i : 0);
+        const float lse2 = row_ok ? __ldg(a.lse + ri) * kLog2e : 0.f;
+        const float dlt = row_ok ? __ldg(a.delta + ri) : 0.f;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s, gs & 1));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          // keys [c0, c0 + kEWCols) of the tile: chunks [qb, qb + kEWCols / 8) of SW128 box hb
+          const int c0 = kEWCols * ew, hb = c0 / 64, qb = (c0 % 64) / 8;
+          constexpr int NC = kEWCols / 8;  // 16-byte chunks per row
+          uint32_t sv[kEWCols], dpv[kEWCols];
 #pragma unroll
-              for (int w = 0; w < 8; ++w)
-                out[(c >> 2) + w] = nsteps > 0 ? make_float4(__uint_as_float(v[4 * w]) * f, __uint_as_float(v[4 * w + 1]) * f,
-                                                             __uint_as_float(v[4 * w + 2]) * f, __uint_as_float(v[4 * w + 3]) * f)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < kEWCols; c += 32) {
+            tmem_ld32(tmem + lane_addr + C::S_COL + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+            tmem_ld32(tmem + lane_addr + C::DP_COL + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(&dpv[c]));
+          }
+          // The row's visible keys in this slice as local columns [vlo, vhi] (empty when
+          // vlo > vhi): a key tile lies in one stream, so one interval of Eq. 2 applies.
+          const int kb = k0 + c0;
+          const bool clean_keys = k0 < a.L;
+          const int vlo = (clean_keys ? 0 : n_lo) - kb;
+          const int vhi = min(clean_keys ? c_hi : n_hi, ke - 1) - kb;
+          const bool full = __all_sync(0xffffffffu, vlo <= 0 && vhi >= kEWCols - 1);  // interior: no mask
+          tc_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bar_sdp);  // S(n), dP(n) are in registers: step n + 1 may overwrite them
+          if (!full) {  // hidden scores become -inf: exp2 of them is exactly 0, and so is dS
+#pragma unroll
+            for (int c = 0; c < kEWCols; ++c) sv[c] = (c >= vlo && c <= vhi) ? sv[c] : 0xFF800000u;
+          }
+          const uint32_t row_off = static_cast<uint32_t>(hb * kBox + r * 128);
+          uint32_t pw[NC][4], dw[NC][4];  // P and dS as bf16 pairs, 8 keys = one 16-byte chunk
+#pragma unroll
+          for (int q = 0; q < NC; ++q) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 8 * q + 2 * e;
+              float x0, x1, d0, d1;
+              fma2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), a.scale_log2, -lse2, x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              sub_mul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, p0, p1, d0, d1);
+              pw[q][e] = pack_bf16x2(p0, p1);
+              dw[q][e] = pack_bf16x2(d0, d1);
             }
           }
-        } else {
-          uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
-          const int H = MODE == kDKV ? a.Hkv : a.Hq;
-          const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
-          uint4* out = reinterpret_cast<uint4*>(dst + (srow * H + hout) * D);
+          // the previous step's accumulating products have read the P / dS tiles
+          if (gs > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree, (gs - 1) & 1));
+          if (!ok) break;
+#pragma unroll
+          for (int q = 0; q < NC; ++q) {
+            const uint32_t sw = static_cast<uint32_t>((((qb + q) ^ (r & 7)) * 16));
+            if (MODE == kDKV) st_shared_v4(p_s + row_off + sw, pw[q][0], pw[q][1], pw[q][2], pw[q][3]);
+            st_shared_v4(ds_s + row_off + sw, dw[q][0], dw[q][1], dw[q][2], dw[q][3]);
+          }
+        }
+        fence_async_smem();  // the generic-proxy stores become visible to the tensor core
+        tc_fence_before();
+        mbar_arrive(&bar_p);
+      }
+      // ---- epilogue: the accumulators (rows = keys for dK, dV; query rows for dQ)
+      if (ok && nsteps > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc, nacc & 1));
+      if (!ok) {
+        if (lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+        break;
+      } else {
+        nacc += nsteps > 0;
+        tc_fence_after();
+        const int row = u0 + r;
+        const bool store = row < uend;
+        const size_t srow = static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0);
+        // The accumulator columns are split evenly over the warpgroups: dK then dV
+        // (dKV mode) or dQ (dQ mode), 16 columns at a time.
+        constexpr int NACC = MODE == kDKV ? 2 : 1;
+        constexpr int SPAN = NACC * D / kEW;  // columns per warpgroup, a multiple of 16
+        static_assert(SPAN % 16 == 0 && D % SPAN == 0, "accumulator split");
+        const int m = (SPAN * ew) / D;
+        const int c_lo = (SPAN * ew) % D, c_hi = c_lo + SPAN;
+        {
+          const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
+          if (MODE == kDKV && a.part != nullptr) {
+            // fp32 partial of this query head, summed over the group by reduce_kernel
+            float4* out = reinterpret_cast<float4*>(a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + srow) *
+                                                                  a.Hq + hh) * D);
 #pragma unroll 1
-          for (int c = c_lo; c < c_hi; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c, v);
-            tc_wait_ld();
-            uint32_t pk[16];
+            for (int c = c_lo; c < c_hi; c += 16) {
+              uint32_t v[16];
+              tmem_ld16(tmem + lane_addr + C::ACC_COL + m * D + c, v);
+              tc_wait_ld();
+              if (store) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f) : 0u;
-            if (store) {
+                for (int w = 0; w < 4; ++w)
+                  out[(c >> 2) + w] = nsteps > 0 ? make_float4(__uint_as_float(v[4 * w]) * f, __uint_as_float(v[4 * w + 1]) * f,
+                                                               __uint_as_float(v[4 * w + 2]) * f, __uint_as_float(v[4 * w + 3]) * f)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+          } else {
+            uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
+            const int H = MODE == kDKV ? a.Hkv : a.Hq;
+            const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
+            uint4* out = reinterpret_cast<uint4*>(dst + (srow * H + hout) * D);
+#pragma unroll 1
+            for (int c = c_lo; c < c_hi; c += 16) {
+              uint32_t v[16];
+              tmem_ld16(tmem + lane_addr + C::ACC_COL + m * D + c, v);
+              tc_wait_ld();
+              uint32_t pk[8];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) out[(c >> 3) + w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+              for (int e = 0; e < 8; ++e)
+                pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f) : 0u;
+              if (store) {
+#pragma unroll
+                for (int w = 0; w < 2; ++w) out[(c >> 3) + w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+              }
             }
           }
         }
@@ -560,8 +682,11 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
   }
   UnitOrder order;
   make_order(a, MODE, &order);
+  BwdArgs am = a;
+  am.next_unit = a.next_unit + MODE;  // one counter per mode
   const long long units = 2LL * a.nt * a.batch * a.Hq;
-  bwd_kernel<D, MODE><<<static_cast<int>(units), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a, order);
+  const int grid = static_cast<int>(std::min<long long>(units, mars_host::num_sms()));  // persistent CTAs
+  bwd_kernel<D, MODE><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, am, order);
   return mars_host::launch_status();
 }
 
@@ -569,15 +694,17 @@ inline size_t align_up(size_t x, size_t al) { return (x + al - 1) / al * al; }
 
 }  // namespace
 
-// Workspace: delta [b, Hq, 2L] fp32, then (GQA only) the dK | dV partials [2][b, 2L, Hq, D] fp32.
+// Workspace: delta [b, Hq, 2L] fp32, the two work counters (256 bytes), then (GQA
+// only) the dK | dV partials [2][b, 2L, Hq, D] fp32.
 inline size_t delta_bytes(int batch, int L, int Hq) {
   return align_up(static_cast<size_t>(batch) * Hq * 2 * L * sizeof(float), 256);
 }
+constexpr size_t kCounterBytes = 256;
 
 extern "C" size_t mars_train_attn_bwd_workspace_size(int batch, int L, int Hq, int Hkv, int D) {
   if (batch <= 0 || L <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
   const size_t part = Hq == Hkv ? 0 : 2 * static_cast<size_t>(batch) * 2 * L * Hq * D * sizeof(float);
-  return delta_bytes(batch, L, Hq) + part;
+  return delta_bytes(batch, L, Hq) + kCounterBytes + part;
 }
 
 extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o,
@@ -590,7 +717,7 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
   MARS_HOST_CHECK(scale > 0.f && scale < INFINITY, MARS_ERR_INVALID_ARG);
   const int nt = (L + kT - 1) / kT;
   MARS_HOST_CHECK(2 * nt <= kMaxTiles, MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(2LL * nt * batch * Hq < (1LL << 31), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(2LL * nt * batch * Hq < (1LL << 30), MARS_ERR_INVALID_ARG);
   const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv};
   for (const void* p : ptrs) MARS_HOST_CHECK(p != nullptr && aligned16(p), MARS_ERR_INVALID_ARG);
   MARS_HOST_CHECK(lse != nullptr && mars_host::aligned4(lse), MARS_ERR_INVALID_ARG);
@@ -604,8 +731,11 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
   BwdArgs a;
   a.lse = lse;
   a.delta = static_cast<const float*>(workspace);
+  int* counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + delta_bytes(batch, L, Hq));
   a.part = Hq == Hkv ? nullptr
-                     : reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(batch, L, Hq));
+                     : reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(batch, L, Hq) +
+                                                kCounterBytes);
+  a.next_unit = counters;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
@@ -626,7 +756,7 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
   delta_kernel<<<static_cast<int>((rows * (D / 8) + 255) / 256), 256, 0, s>>>(o, dout, static_cast<float*>(workspace),
-                                                                              batch, 2 * L, Hq, D);
+                                                                              counters, batch, 2 * L, Hq, D);
   rc = mars_host::launch_status();
   if (rc != MARS_OK) return rc;
   rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, s);
