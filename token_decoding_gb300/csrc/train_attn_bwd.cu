@@ -66,15 +66,19 @@ template <int D, int MODE>
 struct BCfg {
   static constexpr int NB = D / 64;
   static constexpr int TILE = NB * kBox;  // one [128 x D] bf16 tile
-  // dKV: the unit's K and V once; a ring of single-tile slots takes dO(n), Q(n),
-  // dO(n + 1), ... in that order.  dQ: the unit's Q and dO once; the ring takes
-  // V(n), K(n), V(n + 1), ...  Both: P (dKV only) and dS [128 x 128] tiles.  A
-  // slot is released by the commit after the last product that reads it, so the
-  // next step's tiles load while this step's products run.
-  static constexpr int NSLOT = (MODE == kDKV && D == 128) ? 3 : 4;  // 3: 225 KB of 227 at D = 128
-  // S(n + 1) ahead of step n's accumulating products needs both tiles of steps n
-  // and n + 1 resident: four slots.  With three, only dP(n + 1) goes ahead.
-  static constexpr bool EARLY_S = NSLOT >= 4;
+  // dKV: the unit's K and V once; one ring of single-tile slots takes dO(n), Q(n),
+  // dO(n + 1), ... in that order.  dQ: the unit's Q and dO once; K and V in two
+  // rings (3 K slots, loaded first, so K(n + 1) waits only for dQ(n - 2); V(n) is
+  // read by dP(n) alone and frees its slot early).  Both: P (dKV only) and dS
+  // [128 x 128] tiles.  A slot is released by the commit after the last product
+  // that reads it, so the next steps' tiles load while this step's products run.
+  static constexpr bool SPLIT = MODE == kDQ;
+  static constexpr int NX = SPLIT ? (D == 128 ? 1 : 2) : 0, NY = SPLIT ? 3 : 0;  // V, K slots (dQ)
+  static constexpr int NSLOT = SPLIT ? NX + NY : (D == 128 ? 3 : 6);  // 3: 225 KB of 227 at D = 128
+  // S(n + 1) ahead of step n's accumulating products needs its tile while step n's
+  // are still held: at least four slots in the single ring; always with two rings.
+  // With three, only dP(n + 1) goes ahead.
+  static constexpr bool EARLY_S = SPLIT || NSLOT >= 4;
   static constexpr int FIXED_OFF = 0;                   // K, V (dKV) or Q, dO (dQ)
   static constexpr int RING_OFF = FIXED_OFF + 2 * TILE;
   static constexpr int P_OFF = RING_OFF + NSLOT * TILE;
@@ -287,11 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t p_s = smem_u32(smem + C::P_OFF);
   const uint32_t ds_s = smem_u32(smem + C::DS_OFF);
   bool ok = true;
+  // Ring slot of step g's tile y (0: dO or V, 1: Q or K) and which fill of that
+  // slot it is (the parity of its barriers).
+  auto slot_of = [&](int g, int y, int& sl, int& k) {
+    if constexpr (C::SPLIT) {
+      sl = y == 0 ? g % C::NX : C::NX + g % C::NY;
+      k = y == 0 ? g / C::NX : g / C::NY;
+    } else {
+      const int tt = 2 * g + y;
+      sl = tt % C::NSLOT;
+      k = tt / C::NSLOT;
+    }
+  };
 
   if (warp == 0) {
     // ================= TMA producer
     if (lane == 0) {
-      int gt = 0;  // ring tiles issued
+      int gp = 0;  // steps whose tiles were issued (over all units)
       Unit U;
       for (int r = 0; ok; ++r) {
         const int u = r == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(a.next_unit, 1);
@@ -319,9 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ot = next_other(U, ot);
           int o0, oe;
           tile_rows(a, ot, o0, oe);
-          for (int y = 0; y < 2; ++y) {  // ring tiles of a step: dO, Q (dKV) or V, K (dQ)
-            const int tt = gt++, sl = tt % C::NSLOT;
-            if (tt >= C::NSLOT && !mbar_wait(&bar_free[sl], ((tt / C::NSLOT) - 1) & 1)) {
+          for (int j = 0; j < 2; ++j) {  // ring tiles of a step: dO, Q (dKV) or K, V (dQ)
+            const int y = C::SPLIT ? 1 - j : j;
+            int sl, k;
+            slot_of(gp, y, sl, k);
+            if (k > 0 && !mbar_wait(&bar_free[sl], (k - 1) & 1)) {
               set_status(a.status, MARS_DEV_TIMEOUT);
               ok = false;
               break;
@@ -332,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&bar_stage[sl], C::TILE);
             for (int c = 0; c < C::NB; ++c) tma_load_4d(dst + c * kBox, tm, &bar_stage[sl], 64 * c, hc, o0, U.b);
           }
+          ++gp;
         }
       }
     }
@@ -346,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Ring tiles of step n: x = 2n (dO or V) and y = 2n + 1 (Q or K); the fixed
     // tiles are the others.
     auto tiles = [&](int n, uint32_t& q_t, uint32_t& do_t, uint32_t& k_t, uint32_t& v_t) {
-      const uint32_t x_t = ring_s + ((2 * n) % C::NSLOT) * C::TILE, y_t = ring_s + ((2 * n + 1) % C::NSLOT) * C::TILE;
+      int sx, sy, kx, ky;
+      slot_of(n, 0, sx, kx);
+      slot_of(n, 1, sy, ky);
+      const uint32_t x_t = ring_s + sx * C::TILE, y_t = ring_s + sy * C::TILE;
       q_t = MODE == kDKV ? y_t : fixed_s;
       do_t = MODE == kDKV ? x_t : fixed_s + C::TILE;
       k_t = MODE == kDKV ? fixed_s : y_t;
@@ -354,8 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // dP(n) = dO V^T (its ring tile x is loaded first)
     auto issue_dp = [&](int n) {
-      const int tx = 2 * n, sx = tx % C::NSLOT;
-      wait_all(&bar_stage[sx], (tx / C::NSLOT) & 1);
+      int sx, kx;
+      slot_of(n, 0, sx, kx);
+      wait_all(&bar_stage[sx], kx & 1);
       if (!ok) return;
       tc_fence_after();
       uint32_t q_t, do_t, k_t, v_t;
@@ -374,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S(n) = Q K^T, then "S(n) and dP(n) ready" (and, after a unit's last step,
     // "the fixed tiles may be replaced")
     auto issue_s = [&](int n, bool unit_last) {
-      const int ty = 2 * n + 1, sy = ty % C::NSLOT;
-      wait_all(&bar_stage[sy], (ty / C::NSLOT) & 1);
+      int sy, ky;
+      slot_of(n, 1, sy, ky);
+      wait_all(&bar_stage[sy], ky & 1);
       if (!ok) return;
       tc_fence_after();
       uint32_t q_t, do_t, k_t, v_t;
@@ -398,7 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_all(&bar_p, n & 1);
       if (!ok) return;
       tc_fence_after();
-      const int sx = (2 * n) % C::NSLOT, sy = (2 * n + 1) % C::NSLOT;
+      int sx, sy, kx, ky;
+      slot_of(n, 0, sx, kx);
+      slot_of(n, 1, sy, ky);
       uint32_t q_t, do_t, k_t, v_t;
       tiles(n, q_t, do_t, k_t, v_t);
       if (leader) {
@@ -527,9 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kEWCols; ++c) sv[c] = (c >= vlo && c <= vhi) ? sv[c] : 0xFF800000u;
           }
           const uint32_t row_off = static_cast<uint32_t>(hb * kBox + r * 128);
-          uint32_t pw[NC][4], dw[NC][4];  // P and dS as bf16 pairs, 8 keys = one 16-byte chunk
-#pragma unroll
-          for (int q = 0; q < NC; ++q) {
+          // One 16-byte chunk (8 keys) of P and dS as bf16 pairs.
+          auto chunk = [&](int q, uint32_t (&pw)[4], uint32_t (&dw)[4]) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c = 8 * q + 2 * e;
@@ -537,18 +562,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               fma2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), a.scale_log2, -lse2, x0, x1);
               const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
               sub_mul2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]), dlt, p0, p1, d0, d1);
-              pw[q][e] = pack_bf16x2(p0, p1);
-              dw[q][e] = pack_bf16x2(d0, d1);
+              pw[e] = pack_bf16x2(p0, p1);
+              dw[e] = pack_bf16x2(d0, d1);
             }
-          }
-          // the previous step's accumulating products have read the P / dS tiles
-          if (gs > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree, (gs - 1) & 1));
-          if (!ok) break;
-#pragma unroll
-          for (int q = 0; q < NC; ++q) {
+          };
+          auto store = [&](int q, const uint32_t (&pw)[4], const uint32_t (&dw)[4]) {
             const uint32_t sw = static_cast<uint32_t>((((qb + q) ^ (r & 7)) * 16));
-            if (MODE == kDKV) st_shared_v4(p_s + row_off + sw, pw[q][0], pw[q][1], pw[q][2], pw[q][3]);
-            st_shared_v4(ds_s + row_off + sw, dw[q][0], dw[q][1], dw[q][2], dw[q][3]);
+            if (MODE == kDKV) st_shared_v4(p_s + row_off + sw, pw[0], pw[1], pw[2], pw[3]);
+            st_shared_v4(ds_s + row_off + sw, dw[0], dw[1], dw[2], dw[3]);
+          };
+          if constexpr (!C::EARLY_S) {
+            // S(n) was issued after step n - 1's accumulating products, so its
+            // completion says the P / dS tiles are free: store as computed.
+#pragma unroll
+            for (int q = 0; q < NC; ++q) {
+              uint32_t pw[4], dw[4];
+              chunk(q, pw, dw);
+              store(q, pw, dw);
+            }
+          } else {
+            uint32_t pw[NC][4], dw[NC][4];
+#pragma unroll
+            for (int q = 0; q < NC; ++q) chunk(q, pw[q], dw[q]);
+            // the previous step's accumulating products have read the P / dS tiles
+            if (gs > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree, (gs - 1) & 1));
+            if (!ok) break;
+#pragma unroll
+            for (int q = 0; q < NC; ++q) store(q, pw[q], dw[q]);
           }
         }
         fence_async_smem();  // the generic-proxy stores become visible to the tensor core
