@@ -20,14 +20,20 @@
 // taken heaviest first by persistent CTAs (one per SM).
 //   warp 0      TMA producer: the item's Q tiles, then K and V tiles (SW128,
 //               64-column boxes) into an NS-stage ring (full/empty mbarriers).
-//   warp 1      TMEM owner and MMA issuer (one thread).  Per key tile n the
-//               tensor pipe runs, in issue order,
+//   warp 1      TMEM owner and MMA issuer (one thread).  At D = 128 it issues
+//               both query tiles' products; per key tile n the tensor pipe
+//               runs, in issue order,
 //                 PV_A(n), S_A(n+1) = Q_A K(n+1)^T, PV_B(n), S_B(n+1),
 //               so while softmax warpgroup A works on S_A the tensor cores
 //               compute B's products, and vice versa.  tcgen05 operations of
 //               one thread execute in order, so S_X(n+1) overwrites the TMEM
 //               columns that PV_X(n) reads only after PV_X(n) has read them,
 //               and the commit after S_X(n+1) also covers PV_X(n).
+//   warp 10     (D = 64 only) a second MMA issuer: warp 1 issues query tile
+//               A's products and warp 10 tile B's, each in its own order
+//               S_X(n+1), PV_X(n), so neither tile's chain waits on the
+//               other's softmax (the issuing warps' own latency per wait and
+//               issue was the step limit with one issuer).
 //   warps 2..5  softmax warpgroup A, warps 6..9 warpgroup B (thread = query
 //               row = TMEM lane): S from TMEM, mask, row max, exp2; P is
 //               written back over S in TMEM as bf16 pairs and PV reads it
@@ -60,10 +66,11 @@ constexpr int kBN = 128;        // keys per tile
 constexpr int kBox = 128 * 128; // bytes of one [128 rows x 64 bf16] SW128 box
 constexpr int kOBox = 32 * 128; // bytes of one [32 rows x 64 bf16] SW128 output box
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
-// 10 warps: TMA producer (warp 0), MMA issuer (warp 1), softmax warpgroups A
-// (warps 2..5) and B (warps 6..9).  Three warps share some SM sub-partitions,
-// which caps the kernel at 168 registers per thread.
-constexpr int kThreads = 320;
+// Warps: TMA producer (warp 0), MMA issuer (warp 1), softmax warpgroups A
+// (warps 2..5) and B (warps 6..9); at D = 64 a second MMA issuer (warp 10)
+// serves warpgroup B.  Three warps share some SM sub-partitions, which caps the
+// kernel at 168 registers per thread.
+constexpr int kIssuerB = 10;
 
 template <int D>
 struct Cfg {
@@ -81,6 +88,10 @@ struct Cfg {
   // warpgroup is computed while its softmax still works on the current tile.  At
   // D = 128 there is no room for it: P is written over S (S_A | S_B | O_A | O_B).
   static constexpr bool SEPP = D == 64;
+  // SEPP: one MMA issuer per query tile (warps 1 and kIssuerB), each running its
+  // own S and PV chain; the K/V stages and the Q tiles are released by both.
+  static constexpr int THREADS = SEPP ? 32 * (kIssuerB + 1) : 320;
+  static constexpr int RELEASES = SEPP ? 2 : 1;
   static constexpr int P_COL = 2 * kBN;  // P_x at P_COL + x * kBN / 2 (bf16 pairs), SEPP only
   static constexpr int O_COL = SEPP ? 3 * kBN : 2 * kBN;
   static_assert(!SEPP || O_COL + 2 * D <= TMEM_COLS, "tensor memory layout");
@@ -203,7 +214,7 @@ __device__ __forceinline__ int nth_item(const Plan& p, const TrainArgs& a, int n
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     train_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const TrainArgs a, const __grid_constant__ Plan plan) {
@@ -217,11 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar_q_full, 1);
-    mbar_init(&bar_q_empty, 1);
+    mbar_init(&bar_q_empty, C::RELEASES);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&bar_k[s], 1);
       mbar_init(&bar_v[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
+      mbar_init(&bar_kv_empty[s], C::RELEASES);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s[x], 1);
@@ -285,8 +296,113 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (C::SEPP && (warp == 1 || warp == kIssuerB)) {
+    // ================= MMA issuer of query tile X (SEPP).  The whole warp runs the
+    // schedule, so the descriptors stay warp-uniform; one elected lane issues the
+    // tcgen05 operations and their commits (a commit tracks its own thread's MMAs,
+    // and one thread's tcgen05 operations execute in issue order).  Per key tile n:
+    //   S_X(n + 1) = Q_X K(n + 1)^T once softmax X has read S_X(n), then
+    //   PV_X(n) once softmax X has stored P_X(n);
+    // the stage of K/V(n) and the Q tiles are released by a commit of each issuer
+    // (barriers of count 2).  Issuer B takes no part in an item with one query tile
+    // beyond releasing what it would have released.
+    const bool leader = elect_one();
+    const int X = warp == 1 ? 0 : 1;
+    constexpr uint32_t id_qk = idesc_bf16(kBM, kBN, false);
+    constexpr uint32_t id_pv = idesc_bf16(kBM, D, true);
+    const uint64_t desc_q = smem_desc(q_s + X * C::Q_BYTES, 16, 1024), desc_k = smem_desc(k_s, 16, 1024);
+    const uint64_t desc_v = smem_desc(v_s, kBox, 1024);
+    const uint32_t s_tm = tmem + X * kBN;
+    const uint32_t p_tm = tmem + C::P_COL + X * (kBN / 2);
+    const uint32_t o_tm = tmem + C::O_COL + X * D;
+    int kt = 0, gs = 0, cp = 0;  // key tiles, S products issued, P phases consumed
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, int parity) { ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity)); };
+    auto issue_s = [&](int st) {
+      if (gs > 0) {
+        wait_all(&bar_sfree[X], (gs - 1) & 1);
+        if (!ok) return;
+        tc_fence_after();
+      }
+      ++gs;
+      const uint64_t kb = desc_k + ((st * C::KV_BYTES) >> 4);
+      if (leader) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * kBox + (ks & 3) * 32) >> 4;
+          tc_mma_ss(s_tm, desc_q + off, kb + off, id_qk, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&bar_s[X]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int st, bool first, bool split) {
+      const uint64_t vb = desc_v + ((st * C::KV_BYTES) >> 4);
+      for (int part = 0; part < (split ? 2 : 1); ++part) {
+        wait_all(&bar_p[X], cp & 1);
+        if (!ok) return;
+        ++cp;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            tc_mma_ts(o_tm, p_tm + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv,
+                      (first && part == 0 && ks == 0) ? 0u : 1u);
+          tc_commit(&bar_pfree[X]);
+        }
+        __syncwarp();
+      }
+    };
+    for (int t = 0, idx; ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
+      const Item it = item_of(a, idx);
+      const int nt = it.sched.count();
+      wait_all(&bar_q_full, t & 1);
+      if (!ok) break;
+      if (X == 1 && !it.two_q) {
+        // nothing to compute: release the Q tiles and each K/V stage once it is
+        // filled (a release before the fill would count toward the previous phase)
+        if (leader) mbar_arrive(&bar_q_empty);
+        for (int n = 0; ok && n < nt; ++n, ++kt) {
+          wait_all(&bar_k[kt % C::NS], (kt / C::NS) & 1);
+          if (ok && leader) mbar_arrive(&bar_kv_empty[kt % C::NS]);
+        }
+        __syncwarp();
+        continue;
+      }
+      wait_all(&bar_k[kt % C::NS], (kt / C::NS) & 1);
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(kt % C::NS);
+      if (!ok) break;
+      if (nt == 1 && leader) tc_commit(&bar_q_empty);
+      for (int n = 0; ok && n < nt; ++n, ++kt) {
+        const int st = kt % C::NS, st1 = (kt + 1) % C::NS;
+        const bool last = n + 1 == nt;
+        int kstart;
+        bool nz, part;
+        it.sched.at(n, kstart, nz, part);
+        const bool split = part && it.j == 0;  // same rule as the softmax warps
+        if (!last) {
+          wait_all(&bar_k[st1], ((kt + 1) / C::NS) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(st1);
+          if (!ok) break;
+          if (n + 2 == nt && leader) tc_commit(&bar_q_empty);  // the item's last S product is issued
+        }
+        issue_pv(st, n == 0, split);  // V(n) arrived with K(n), awaited before S(n)
+        if (!ok) break;
+        if (leader) {
+          if (last) tc_commit(&bar_o[X]);
+          tc_commit(&bar_kv_empty[st]);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && leader) set_status(a.status, MARS_DEV_TIMEOUT);
+    __syncwarp();
   } else if (warp == 1) {
-    // ================= MMA issuer.  The whole warp runs the schedule, so the
+    // ================= MMA issuer (D = 128).  The whole warp runs the schedule, so the
     // descriptors stay warp-uniform; one elected lane issues the tcgen05
     // operations and their commits (a commit tracks its own thread's MMAs).
     {
@@ -344,76 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      // SEPP schedule: S_x(n + 1) as soon as the softmax has read S_x(n), then PV_x(n)
-      // from the separate P_x (a split tile is two PVs through P_x: hi, then lo).
-      int gs[2] = {0, 0};  // S products issued per query tile (SEPP)
-      auto issue_s_sep = [&](int x, int st) {
-        if (gs[x] > 0) {
-          wait_all(&bar_sfree[x], (gs[x] - 1) & 1);
-          if (!ok) return;
-          tc_fence_after();
-        }
-        ++gs[x];
-        issue_qk(x, st);
-      };
-      auto issue_pv_sep = [&](int x, int st, bool first, bool split) {
-        const uint32_t p_col = tmem + C::P_COL + x * (kBN / 2);
-        const uint32_t o_col = tmem + C::O_COL + x * D;
-        const uint64_t vb = desc_v + ((st * C::KV_BYTES) >> 4);
-        for (int part = 0; part < (split ? 2 : 1); ++part) {
-          wait_all(&bar_p[x], cp[x] & 1);
-          if (!ok) return;
-          ++cp[x];
-          tc_fence_after();
-          if (leader) {
-#pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks)
-              tc_mma_ts(o_col, p_col + ks * 8, vb + ((ks * 16 * 128) >> 4), id_pv,
-                        (first && part == 0 && ks == 0) ? 0u : 1u);
-            tc_commit(&bar_pfree[x]);
-          }
-          __syncwarp();
-        }
-      };
-      for (int idx; C::SEPP && ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
-        const Item it = item_of(a, idx);
-        const int nt = it.sched.count();
-        wait_all(&bar_q_full, t & 1);
-        wait_all(&bar_k[kt % C::NS], (kt / C::NS) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s_sep(0, kt % C::NS);
-        if (it.two_q) issue_s_sep(1, kt % C::NS);
-        if (!ok) break;
-        if (nt == 1) commit(&bar_q_empty);
-        for (int n = 0; ok && n < nt; ++n, ++kt) {
-          const int st = kt % C::NS, st1 = (kt + 1) % C::NS;
-          const bool last = n + 1 == nt;
-          int kstart;
-          bool nz, part;
-          it.sched.at(n, kstart, nz, part);
-          const bool split = part && it.j == 0;  // same rule as the softmax warps
-          if (!last) {
-            wait_all(&bar_k[st1], ((kt + 1) / C::NS) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s_sep(0, st1);
-            if (it.two_q) issue_s_sep(1, st1);
-            if (!ok) break;
-            if (n + 2 == nt) commit(&bar_q_empty);  // the item's last S products are issued
-          }
-          issue_pv_sep(0, st, n == 0, split);  // V(n) arrived with K(n), awaited before S(n)
-          if (!ok) break;
-          if (last) commit(&bar_o[0]);
-          if (it.two_q) {
-            issue_pv_sep(1, st, n == 0, split);
-            if (!ok) break;
-            if (last) commit(&bar_o[1]);
-          }
-          commit(&bar_kv_empty[st]);
-        }
-      }
-      for (int idx; !C::SEPP && ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
+      for (int idx; ok && (idx = nth_item(plan, a, t)) >= 0; ++t) {
         const Item it = item_of(a, idx);
         const int nt = it.sched.count();
         wait_all(&bar_q_full, t & 1);
@@ -798,7 +845,7 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
   static Plan none;  // unused when a.planned == 0
   const Plan* plan = plan_for(a, D, grid);
   a.planned = plan != nullptr ? 1 : 0;
-  train_attn_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(tq, tk, tv, to, a, plan != nullptr ? *plan : none);
+  train_attn_kernel<D><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM, stream>>>(tq, tk, tv, to, a, plan != nullptr ? *plan : none);
   return mars_host::launch_status();
 }
 
