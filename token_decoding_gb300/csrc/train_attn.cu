@@ -558,8 +558,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           mbar_arrive(&bar_sfree[x]);  // S_x is in registers: the next S may overwrite it
         }
         if (part) {
+          // the row's visible columns as one bit mask per 32 columns, then one bit
+          // test and select per score (cheaper than two compares per score)
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) v0[c] = (c >= vlo && c <= vhi) ? v0[c] : 0xFF800000u;
+          for (int q = 0; q < kBN / 32; ++q) {
+            const int lo = min(max(vlo - 32 * q, 0), 32), hi = min(max(vhi - 32 * q + 1, 0), 32);
+            const uint32_t below_hi = hi >= 32 ? 0xffffffffu : (1u << hi) - 1u;
+            const uint32_t below_lo = lo >= 32 ? 0xffffffffu : (1u << lo) - 1u;
+            const uint32_t m = below_hi & ~below_lo;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v0[32 * q + c] = ((m >> c) & 1u) ? v0[32 * q + c] : 0xFF800000u;
+          }
         }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll

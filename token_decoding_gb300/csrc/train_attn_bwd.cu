@@ -50,6 +50,7 @@ constexpr int kT = 128;            // query rows of a query tile = keys of a key
 constexpr int kBox = 128 * 128;    // bytes of one [128 rows x 64 bf16] SW128 box
 constexpr int kEW = 2;             // elementwise warpgroups, each 128 / kEW keys of a step
 constexpr int kEWCols = kT / kEW;
+static_assert(kEWCols % 32 == 0, "the visibility mask is built per 32 columns");
 constexpr int kThreads = 64 + 128 * kEW;  // producer, MMA issuer, elementwise warps
 constexpr int kMaxTiles = 1024;    // tiles per batch entry and head (2 * ceil(L / 128))
 
@@ -549,8 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar_sdp);  // S(n), dP(n) are in registers: step n + 1 may overwrite them
           if (!full) {  // hidden scores become -inf: exp2 of them is exactly 0, and so is dS
+            // the visible columns as one bit mask per 32 columns, then one bit test and
+            // select per score (cheaper than two compares per score)
 #pragma unroll
-            for (int c = 0; c < kEWCols; ++c) sv[c] = (c >= vlo && c <= vhi) ? sv[c] : 0xFF800000u;
+            for (int q = 0; q < kEWCols / 32; ++q) {
+              const int lo = min(max(vlo - 32 * q, 0), 32), hi = min(max(vhi - 32 * q + 1, 0), 32);
+              const uint32_t below_hi = hi >= 32 ? 0xffffffffu : (1u << hi) - 1u;
+              const uint32_t below_lo = lo >= 32 ? 0xffffffffu : (1u << lo) - 1u;
+              const uint32_t m = below_hi & ~below_lo;
+#pragma unroll
+              for (int c = 0; c < 32; ++c) sv[32 * q + c] = ((m >> c) & 1u) ? sv[32 * q + c] : 0xFF800000u;
+            }
           }
           const uint32_t row_off = static_cast<uint32_t>(hb * kBox + r * 128);
           // One 16-byte chunk (8 keys) of P and dS as bf16 pairs.
