@@ -795,8 +795,20 @@ bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// LPT plan for (shape, grid), cached: item cost = key tiles (x 0.6 for a single-head
-// item) + a per-item overhead of about 2.5 tiles, all in tenths of a tile.
+// Work plan for (shape, grid), cached.  Item cost model, fitted by least squares to
+// per-item durations measured on GB300 (globaltimer at each item's epilogue, both
+// training shapes; 7-8% rms error per item), in units of 0.01 us:
+//   key tiles x (two query tiles ? c2 : c1) + partial tiles of a one-head item x p1
+//   + per item o + (first query tile of a stream: the hi/lo split) key tiles x sp.
+// Items are assigned longest-processing-time first, then the most loaded CTA gives
+// up an item (or trades one for a cheaper one) while that lowers its load: with only
+// ~3-4 items per CTA, LPT alone leaves the slowest CTA ~10% above the mean.
+struct CostModel {
+  int c2, c1, p1, o, sp;
+};
+constexpr CostModel kCost64 = {160, 91, 52, 27, 94};
+constexpr CostModel kCost128 = {176, 139, 86, 15, 132};
+
 const Plan* plan_for(const TrainArgs& a, int D, int grid) {
   if (grid > kMaxPlanCtas || a.items > kMaxPlanItems) return nullptr;
   struct Entry {
@@ -809,10 +821,17 @@ const Plan* plan_for(const TrainArgs& a, int D, int grid) {
   std::lock_guard<std::mutex> lock(mu);
   for (const Entry& e : cache)
     if (std::equal(key, key + 8, e.key)) return e.plan.get();
-  std::vector<int> cost(a.items), order(a.items);
+  const CostModel cm = D == 64 ? kCost64 : kCost128;
+  std::vector<long long> cost(a.items);
+  std::vector<int> order(a.items);
   for (int i = 0; i < a.items; ++i) {
     const Item it = item_of(a, i);
-    cost[i] = it.sched.count() * (it.two_q ? 10 : 6) + 25;
+    const Sched& sc = it.sched;
+    const int tiles = sc.count(), partial = (sc.n_clean - sc.clean_full) + sc.n_noisy;
+    long long c = static_cast<long long>(tiles) * (it.two_q ? cm.c2 : cm.c1) + cm.o;
+    if (!it.two_q) c += static_cast<long long>(partial) * cm.p1;
+    if (it.j == 0) c += static_cast<long long>(tiles) * cm.sp;
+    cost[i] = c;
     order[i] = i;
   }
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
@@ -825,9 +844,53 @@ const Plan* plan_for(const TrainArgs& a, int D, int grid) {
     load[best] += cost[i];
     lists[best].push_back(i);
   }
+  // refinement: a bounded number of improving moves / swaps off the most loaded CTA
+  if (a.items <= 8 * grid) {
+    for (int iter = 0; iter < 4 * grid; ++iter) {
+      int hi = 0;
+      for (int c = 1; c < grid; ++c)
+        if (load[c] > load[hi]) hi = c;
+      long long best_max = load[hi];
+      int best_lo = -1, best_a = -1, best_b = -1;  // best_b < 0: move
+      for (int lo = 0; lo < grid; ++lo) {
+        if (lo == hi) continue;
+        for (int ia = 0; ia < static_cast<int>(lists[hi].size()); ++ia) {
+          const long long ca = cost[lists[hi][ia]];
+          const long long mv = std::max(load[hi] - ca, load[lo] + ca);
+          if (mv < best_max) {
+            best_max = mv;
+            best_lo = lo, best_a = ia, best_b = -1;
+          }
+          for (int ib = 0; ib < static_cast<int>(lists[lo].size()); ++ib) {
+            const long long d = ca - cost[lists[lo][ib]];
+            if (d <= 0) continue;
+            const long long sw = std::max(load[hi] - d, load[lo] + d);
+            if (sw < best_max) {
+              best_max = sw;
+              best_lo = lo, best_a = ia, best_b = ib;
+            }
+          }
+        }
+      }
+      if (best_lo < 0) break;
+      const int ia = lists[hi][best_a];
+      lists[hi].erase(lists[hi].begin() + best_a);
+      lists[best_lo].push_back(ia);
+      load[hi] -= cost[ia];
+      load[best_lo] += cost[ia];
+      if (best_b >= 0) {
+        const int ib = lists[best_lo][best_b];
+        lists[best_lo].erase(lists[best_lo].begin() + best_b);
+        lists[hi].push_back(ib);
+        load[best_lo] -= cost[ib];
+        load[hi] += cost[ib];
+      }
+    }
+  }
   std::unique_ptr<Plan> p(new Plan());
   int j = 0;
   for (int c = 0; c < grid; ++c) {
+    std::sort(lists[c].begin(), lists[c].end(), [&](int x, int y) { return cost[x] > cost[y]; });
     p->start[c] = static_cast<uint16_t>(j);
     for (int i : lists[c]) p->item[j++] = static_cast<uint16_t>(i);
   }
