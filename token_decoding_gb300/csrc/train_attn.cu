@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // launched as a programmatic dependent: set-up above overlaps the previous kernel,
+  // nothing global is touched before it has completed
+  griddep_wait();
 
   const uint32_t q_s = smem_u32(smem + C::Q_OFF);
   const uint32_t k_s = smem_u32(smem + C::K_OFF);
@@ -753,6 +756,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (!ok && lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
   }
 
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -917,8 +921,18 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
   static Plan none;  // unused when a.planned == 0
   const Plan* plan = plan_for(a, D, grid);
   a.planned = plan != nullptr ? 1 : 0;
-  train_attn_kernel<D><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM, stream>>>(tq, tk, tv, to, a, plan != nullptr ? *plan : none);
-  return mars_host::launch_status();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(Cfg<D>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, train_attn_kernel<D>, tq, tk, tv, to, a, plan != nullptr ? *plan : none);
+  return e == cudaSuccess ? MARS_OK : mars_host::cuda_fail(e);
 }
 
 }  // namespace
