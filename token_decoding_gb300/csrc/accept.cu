@@ -286,6 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
   }
   __syncthreads();
   griddep_launch_dependents();  // the finish launch may start prefetching beside us
+  // launched as a programmatic dependent of whatever precedes it in the stream: the
+  // set-up above overlaps that kernel, the logits are read only once it has completed
+  griddep_wait();
 
   if (warp == kSlots) {
     // ================= producer: the CTA's chunks, in order, through the ring
@@ -476,11 +479,21 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
   a.chunks = chunks_for(a.V);
   a.items = a.batch * a.B * a.chunks;
   const int grid = std::min(a.items, mars_host::num_sms());
-  if (a.margin)
-    accept_kernel<true><<<grid, kThreads, kRingBytes, stream>>>(a);
-  else
-    accept_kernel<false><<<grid, kThreads, kRingBytes, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return mars_host::launch_status();
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kRingBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = a.margin ? cudaLaunchKernelEx(&cfg, accept_kernel<true>, a)
+                                   : cudaLaunchKernelEx(&cfg, accept_kernel<false>, a);
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
+  }
   // The finish launch overlaps its start-up and prefetch with the streaming launch
   // (programmatic dependent launch); it waits for the partials in-kernel.
   cudaLaunchConfig_t cfg = {};

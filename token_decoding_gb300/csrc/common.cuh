@@ -330,6 +330,22 @@ __device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr) {
 
 // Host helpers shared by the entry points.
 namespace mars_host {
+// Launch configuration for a programmatic dependent launch (the kernel calls
+// griddep_wait() before touching global memory): pdl_attr fills one attribute.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cfg;
+}
+inline void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1]) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
 int check_device();  // MARS_OK or MARS_ERR_UNSUPPORTED_DEVICE / MARS_ERR_CUDA (cached per device)
 int num_sms();       // SM count of the current device (cached)
 int cuda_fail(cudaError_t e);  // records e for mars_last_cuda_error(); returns MARS_ERR_CUDA

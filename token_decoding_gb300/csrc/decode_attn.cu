@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  // launched as a programmatic dependent: nothing global is read before the previous
+  // kernel in the stream has completed
+  griddep_wait();
 
   // ---- which sequence: heavy-first rank order (stable by index) or plain order
   const int b_rank = unit_rank / units_per_b;
@@ -614,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     __syncthreads();  // every tensor-memory read of the epilogue is done
   }
+  griddep_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -673,13 +677,15 @@ int launch(const Maps& mp, const DecodeArgs& a, int units, cudaStream_t stream) 
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = DCfg<D>::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mp.q, mp.kc, mp.vc, mp.kn, mp.vn, a);
   if (e != cudaSuccess) return mars_host::cuda_fail(e);
   return MARS_OK;

@@ -152,6 +152,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 __global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                                     float* __restrict__ delta, int* __restrict__ counters, int batch,
                                                     int n2, int Hq, int D) {
+  // launched as a programmatic dependent: nothing global is touched before the
+  // previous kernel in the stream has completed; the next kernel may start its set-up
+  griddep_wait();
+  griddep_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x < 2) counters[threadIdx.x] = 0;  // the two work counters of bwd_kernel
   const int per_row = D / 8;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -184,6 +188,8 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__
 __global__ void __launch_bounds__(256) reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ dk,
                                                      uint16_t* __restrict__ dv, int batch, int n2, int Hkv, int G,
                                                      int D) {
+  griddep_wait();  // programmatic dependent launch, as delta_kernel
+  griddep_launch_dependents();
   const long long e8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long per_m = static_cast<long long>(batch) * n2 * Hkv * D / 8;
   if (e8 >= 2 * per_m) return;
@@ -287,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // programmatic dependent launch: the set-up above overlaps the previous kernel;
+  // nothing global (inputs, work counter, outputs) is touched before it has completed
+  griddep_wait();
   const uint32_t fixed_s = smem_u32(smem + C::FIXED_OFF);
   const uint32_t ring_s = smem_u32(smem + C::RING_OFF);
   const uint32_t p_s = smem_u32(smem + C::P_OFF);
@@ -666,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -736,8 +746,11 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
   am.next_unit = a.next_unit + MODE;  // one counter per mode
   const long long units = 2LL * a.nt * a.batch * a.Hq;
   const int grid = static_cast<int>(std::min<long long>(units, mars_host::num_sms()));  // persistent CTAs
-  bwd_kernel<D, MODE><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, am, order);
-  return mars_host::launch_status();
+  cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(grid), dim3(kThreads), C::SMEM, stream);
+  cudaLaunchAttribute attr[1];
+  mars_host::pdl_attr(cfg, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_kernel<D, MODE>, tq, tk, tv, tdo, am, order);
+  return e == cudaSuccess ? MARS_OK : mars_host::cuda_fail(e);
 }
 
 inline size_t align_up(size_t x, size_t al) { return (x + al - 1) / al * al; }
@@ -805,17 +818,25 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
     return MARS_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
-  delta_kernel<<<static_cast<int>((rows * (D / 8) + 255) / 256), 256, 0, s>>>(o, dout, static_cast<float*>(workspace),
-                                                                              counters, batch, 2 * L, Hq, D);
-  rc = mars_host::launch_status();
-  if (rc != MARS_OK) return rc;
+  {
+    cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(static_cast<int>((rows * (D / 8) + 255) / 256)), dim3(256), 0, s);
+    cudaLaunchAttribute attr[1];
+    mars_host::pdl_attr(cfg, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, delta_kernel, static_cast<const uint16_t*>(o),
+                                             static_cast<const uint16_t*>(dout), static_cast<float*>(workspace),
+                                             counters, batch, 2 * L, Hq, D);
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
+  }
   rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, s);
   if (rc != MARS_OK) return rc;
   if (a.part != nullptr) {
     const long long e8 = 2LL * batch * 2 * L * Hkv * D / 8;
-    reduce_kernel<<<static_cast<int>((e8 + 255) / 256), 256, 0, s>>>(a.part, dk, dv, batch, 2 * L, Hkv, a.G, D);
-    rc = mars_host::launch_status();
-    if (rc != MARS_OK) return rc;
+    cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(static_cast<int>((e8 + 255) / 256)), dim3(256), 0, s);
+    cudaLaunchAttribute attr[1];
+    mars_host::pdl_attr(cfg, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel, static_cast<const float*>(a.part), dk, dv, batch,
+                                             2 * L, Hkv, a.G, D);
+    if (e != cudaSuccess) return mars_host::cuda_fail(e);
   }
   return D == 64 ? launch<64, kDQ>(tq, tk, tv, tdo, a, s) : launch<128, kDQ>(tq, tk, tv, tdo, a, s);
 }
