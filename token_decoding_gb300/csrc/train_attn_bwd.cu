@@ -293,9 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // programmatic dependent launch: the set-up above overlaps the previous kernel;
-  // nothing global (inputs, work counter, outputs) is touched before it has completed
-  griddep_wait();
+  // Programmatic dependent launch: the set-up above overlaps the previous kernel.
+  // The dK/dV pass touches nothing global before that kernel has completed.  The dQ
+  // pass reads only what delta_kernel and the caller wrote: it starts once the
+  // kernel before it (the GQA reduction, or the dK/dV pass) has released its
+  // dependents, which each does after its own wait, so those writes are complete;
+  // the dQ pass waits at its end instead, so it runs beside the reduction and still
+  // completes after it.
+  if constexpr (MODE == kDKV) griddep_wait();
   const uint32_t fixed_s = smem_u32(smem + C::FIXED_OFF);
   const uint32_t ring_s = smem_u32(smem + C::RING_OFF);
   const uint32_t p_s = smem_u32(smem + C::P_OFF);
@@ -675,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if constexpr (MODE == kDQ) griddep_wait();
   griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
