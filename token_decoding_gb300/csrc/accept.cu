@@ -285,10 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1) accept_kernel(const AcceptArgs a)
     fence_mbar_init();
   }
   __syncthreads();
-  griddep_launch_dependents();  // the finish launch may start prefetching beside us
-  // launched as a programmatic dependent of whatever precedes it in the stream: the
-  // set-up above overlaps that kernel, the logits are read only once it has completed
+  // Launched as a programmatic dependent of whatever precedes it in the stream: the
+  // set-up above overlaps that kernel, and nothing global is read before it has
+  // completed.  Only then may the finish launch start: it prefetches the candidate
+  // K/V rows, which that kernel may have written, before it waits for this one.
   griddep_wait();
+  griddep_launch_dependents();  // the finish launch may start prefetching beside us
 
   if (warp == kSlots) {
     // ================= producer: the CTA's chunks, in order, through the ring
