@@ -17,8 +17,12 @@
  *   vector, cp.async and TMA accesses), except `logits`, which needs only 2-byte
  *   alignment; int32 / fp32 arrays need 4-byte alignment.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- *   stream) and never allocate, free or synchronise.  They can be captured in a
- *   CUDA graph.
+ *   stream) and never allocate, free or synchronise.  The calls other than
+ *   mars_accept_noalloc can be captured in a CUDA graph.
+ * - Kernels are launched as programmatic dependent launches: their set-up may
+ *   overlap the tail of the previous kernel in the stream, but none of them
+ *   touches global memory before that kernel has completed, so stream order
+ *   holds as for plain launches.
  * - The return value reports what the host can see before launch; conditions
  *   that only the device can see are OR-ed into the optional device status
  *   word (`int32_t*` in device memory, may be NULL), which the caller reads
