@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(32 * 16) accept_finish_kernel(const AcceptArgs
     }
   }
   griddep_wait();  // the streaming launch's partials are complete and visible from here on
+  griddep_launch_dependents();  // the next kernel (a decode step) may start its set-up
   {
     const int r = b * a.B + warp;
     RowState mg = empty_state();
