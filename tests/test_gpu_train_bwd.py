@@ -82,14 +82,32 @@ def test_group_of_seven_d128():
     case(1, 256, 4, 7, 1, 128, 3400)
 
 
-def test_qwen05b_shape_one_group():
+def _shape_groups(s, seed, groups):
+    """The full-size backward once on the GPU, then (sequence, KV group) slices
+    against the oracle: a group's query heads only touch their own KV head."""
+    q = rand_bf16((s.batch, 2 * s.L, s.Hq, s.D), seed)
+    k, v = rand_bf16((s.batch, 2 * s.L, s.Hkv, s.D), seed + 1), rand_bf16((s.batch, 2 * s.L, s.Hkv, s.D), seed + 2)
+    do = rand_bf16((s.batch, 2 * s.L, s.Hq, s.D), seed + 3)
+    scale = s.D ** -0.5
+    dq, dk, dv = run(q, k, v, do, s.L, s.B, scale)
+    G = s.Hq // s.Hkv
+    for b, g in groups:
+        hs = slice(g * G, (g + 1) * G)
+        want = oracle.train_attn_bwd(q.f64[b:b + 1, :, hs], k.f64[b:b + 1, :, g:g + 1], v.f64[b:b + 1, :, g:g + 1],
+                                     do.f64[b:b + 1, :, hs], s.L, s.B, scale)
+        got = (dq[b:b + 1, :, hs], dk[b:b + 1, :, g:g + 1], dv[b:b + 1, :, g:g + 1])
+        for x, w, n in zip(got, want, ("dq", "dk", "dv")):
+            check(x, w, f"{n} b{b} g{g}")
+
+
+def test_qwen05b_shape_every_group():
     s = synth.TRAIN_05B
-    case(s.batch, s.L, s.B, s.Hq, s.Hkv, s.D, 3500, heads=(3, 1))
+    _shape_groups(s, 3500, [(b, g) for b in range(s.batch) for g in range(s.Hkv)])
 
 
-def test_qwen7b_shape_one_group():
+def test_qwen7b_shape_two_groups():
     s = synth.TRAIN_7B
-    case(s.batch, s.L, s.B, s.Hq, s.Hkv, s.D, 3600, heads=(1, 2))
+    _shape_groups(s, 3600, [(0, 0), (1, 2)])
 
 
 def test_deterministic():

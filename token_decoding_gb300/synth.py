@@ -211,3 +211,40 @@ def step_logits(shape: DecodeShape, step: int, seed_key=0, spike_lo=None, spike_
         exact = shape.B // 2
     return spiked_logits(shape.batch, shape.B, shape.V, shape.base_sigma, shape.spike_prob,
                          lo, hi, g, exact_spike_count=exact)
+
+
+# --------------------------------------------------------------------------
+# Per-sequence draws (sliding-window episodes checked on a subset of sequences)
+# --------------------------------------------------------------------------
+# Sequences of a decode batch are independent, so an episode can be checked on
+# a few of them: these generators draw one sequence's arrays from a seed of its
+# own (workload, sequence, step), so that the sequences under check never need
+# the whole batch drawn on the host.
+
+def seq_cache_inputs(shape: DecodeShape, b: int, fill_len: int, seed_key=0):
+    """k_cache, v_cache [1, Hkv, cap, D] of sequence b; rows past fill_len are zero."""
+    g = rng_for("seq_cache", shape.name, seed_key, b)
+    kc = np.zeros((1, shape.Hkv, shape.cap, shape.D), dtype=np.float32)
+    vc = np.zeros_like(kc)
+    kc[:, :, :fill_len, :] = g.standard_normal((1, shape.Hkv, fill_len, shape.D), dtype=np.float32)
+    vc[:, :, :fill_len, :] = g.standard_normal((1, shape.Hkv, fill_len, shape.D), dtype=np.float32)
+    return Bf16.from_float(kc), Bf16.from_float(vc)
+
+
+def seq_step_inputs(shape: DecodeShape, step: int, b: int, seed_key=0):
+    """This step's q [1, B, Hq, D], k_new, v_new [1, B, Hkv, D] of sequence b."""
+    g = rng_for("seq_step", shape.name, seed_key, step, b)
+    q = Bf16.from_float(g.standard_normal((1, shape.B, shape.Hq, shape.D), dtype=np.float32))
+    kn = Bf16.from_float(g.standard_normal((1, shape.B, shape.Hkv, shape.D), dtype=np.float32))
+    vn = Bf16.from_float(g.standard_normal((1, shape.B, shape.Hkv, shape.D), dtype=np.float32))
+    return q, kn, vn
+
+
+def seq_step_logits(shape: DecodeShape, step: int, b: int, seed_key=0, spike_lo=None, spike_hi=None,
+                    spike_prob=None):
+    """This step's logits [1, B, V] of sequence b (the workload's spike recipe unless overridden)."""
+    g = rng_for("seq_logits", shape.name, seed_key, step, b)
+    lo = shape.spike_lo if spike_lo is None else spike_lo
+    hi = shape.spike_hi if spike_hi is None else spike_hi
+    prob = shape.spike_prob if spike_prob is None else spike_prob
+    return spiked_logits(1, shape.B, shape.V, shape.base_sigma, prob, lo, hi, g)
