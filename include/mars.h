@@ -48,6 +48,8 @@ extern "C" {
 #define MARS_ERR_CUDA 3                /* a CUDA runtime call or a launch failed */
 #define MARS_ERR_UNSUPPORTED_DEVICE 4  /* current device is not compute capability 10.3 */
 #define MARS_ERR_SCRATCH_LIMIT 5       /* shape too large for mars_accept_noalloc's fixed scratch */
+#define MARS_ERR_SCRATCH_NOT_READY 6   /* mars_accept_noalloc's first call in a CUDA context came during a stream
+                                          capture; make one call outside capture first */
 
 /* Bits that kernels OR into the device status word. */
 #define MARS_DEV_CAPACITY 1   /* mars_accept: cache_len + n_commit would exceed cap; that sequence was not appended;
@@ -302,9 +304,11 @@ int mars_accept_margin(const uint16_t* logits, int batch, int B, int V, float ta
  *   - Limit: batch * B * ceil(V / 8192) <= 65536 (one partial result per
  *     16 KB slice of logits must fit); larger shapes return
  *     MARS_ERR_SCRATCH_LIMIT without launching anything.
- *   - The first call on a device sets the scratch up on that device (it looks
- *     up the array's device address); make that first call before any stream
- *     capture begins.
+ *   - The first call in each CUDA context (per device; again after a
+ *     cudaDeviceReset) sets the scratch up: it looks up the array's device
+ *     address with that device current.  Make that first call before any
+ *     stream capture begins: a first call on a stream that is being captured
+ *     returns MARS_ERR_SCRATCH_NOT_READY and launches nothing.
  *   - All calls in the process share the one array per device and it keeps
  *     the last call's contents; calls that overlap on the GPU (for example on
  *     two streams at once) race on it and must be serialised by the caller.
@@ -315,6 +319,27 @@ int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int V, float t
                         int Hkv, int D, int cap,
                         int32_t* tokens, float* conf, int32_t* n_commit,
                         int32_t* status, void* stream);
+
+/*
+ * mars_selftest_wait_timeout - runs, on the device, the bounded pipeline wait
+ * that every kernel of this library uses, on a barrier that needs two arrivals.
+ * The MARS pages have no counterpart: this checks the library's own failure
+ * path without faulting, trapping or hanging the GPU.
+ *
+ *   withhold_arrival  nonzero: the second arrival never comes, so the wait
+ *                     gives up after spin_limit polls; nothing asynchronous
+ *                     (no copy, no tensor-core commit) targets the barrier
+ *   spin_limit        polls before the wait gives up, 1 .. 2^24 (the kernels'
+ *                     own limit is the maximum)
+ *   status           device int32 word: MARS_DEV_TIMEOUT is OR-ed in when the
+ *                     wait gave up (required)
+ *   elapsed_ns       device uint64 (8-byte aligned, may be NULL): nanoseconds
+ *                     the wait took (%globaltimer)
+ * The kernel holds tensor memory across the wait and frees it afterwards, as
+ * the real kernels do when a wait gives up, so the context stays usable.
+ */
+int mars_selftest_wait_timeout(int withhold_arrival, unsigned int spin_limit, int32_t* status,
+                               unsigned long long* elapsed_ns, void* stream);
 
 #ifdef __cplusplus
 }

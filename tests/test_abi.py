@@ -27,7 +27,7 @@ def lib():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "mars_accept", "mars_accept_ex", "mars_accept_margin", "mars_accept_noalloc", "mars_accept_workspace_size",
-        "mars_decode_attn", "mars_decode_attn_deferred", "mars_last_cuda_error",
+        "mars_decode_attn", "mars_decode_attn_deferred", "mars_last_cuda_error", "mars_selftest_wait_timeout",
         "mars_train_attn_bwd", "mars_train_attn_bwd_workspace_size", "mars_status_string", "mars_train_attn", "mars_version"])
 
 
@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     lib.mars_status_string.restype = ctypes.c_char_p
-    for code in range(6):
+    for code in range(7):
         assert lib.mars_status_string(code)
     assert b"unknown" in lib.mars_status_string(99)
     assert lib.mars_version() == 100

@@ -83,6 +83,49 @@ def test_noalloc_matches_workspace_accept_twice(batch, B, V, tau):
         assert np.array_equal(bits_of(vc_a)[same], bits_of(vc_b)[same])
 
 
+def test_noalloc_large_then_small_without_reset():
+    """A small call right after a large one reads only slots it wrote itself: the
+    stale partials the large call left in the shared array change nothing."""
+    tau = 0.5
+    big = _inputs(64, 8, 152064, 4, 128, 64, "big")
+    small = _inputs(3, 5, 1001, 4, 128, 64, "small")
+    for logits, kn, vn, kc, vc, lens in (big, small):
+        d_logits, d_kn, d_vn = dev_bf16(logits), dev_bf16(kn), dev_bf16(vn)
+        kc_a, vc_a, len_a = _state(kc, vc, lens)
+        tok_a, conf_a, n_a = mars.accept(d_logits, tau, d_kn, d_vn, kc_a, vc_a, len_a)
+        nb, B = logits.shape[:2]
+        kc_b, vc_b, len_b = _state(kc, vc, lens)
+        tok_b = torch.full((nb, B), -1, dtype=torch.int32, device="cuda")
+        conf_b = torch.full((nb, B), -1.0, dtype=torch.float32, device="cuda")
+        n_b = torch.full((nb,), -1, dtype=torch.int32, device="cuda")
+        _noalloc_via_c_abi(d_logits, tau, d_kn, d_vn, kc_b, vc_b, len_b, tok_b, conf_b, n_b)
+        torch.cuda.synchronize()
+        assert torch.equal(tok_a, tok_b)
+        ca, cb = conf_a.cpu().numpy().astype(np.float64), conf_b.cpu().numpy().astype(np.float64)
+        assert float(np.max(np.abs(ca - cb) / ca)) < 1e-5
+        assert torch.equal(n_a, n_b) or bool((np.abs(ca - tau) < 1e-4).any())
+
+
+def test_noalloc_python_wrapper_with_status_word():
+    """The binding's accept_noalloc passes its arguments in the C order and leaves a
+    clean status word (0) on a valid call."""
+    logits, kn, vn, kc, vc, lens = _inputs(2, 4, 5000, 2, 64, 48, "wrapper")
+    d_logits, d_kn, d_vn = dev_bf16(logits), dev_bf16(kn), dev_bf16(vn)
+    kc_a, vc_a, len_a = _state(kc, vc, lens)
+    tok_a, conf_a, n_a = mars.accept(d_logits, 0.4, d_kn, d_vn, kc_a, vc_a, len_a)
+    kc_b, vc_b, len_b = _state(kc, vc, lens)
+    tok_b = torch.empty((2, 4), dtype=torch.int32, device="cuda")
+    conf_b = torch.empty((2, 4), dtype=torch.float32, device="cuda")
+    n_b = torch.empty((2,), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _lib.accept_noalloc(d_logits, 0.4, d_kn, d_vn, kc_b, vc_b, len_b, tok_b, conf_b, n_b, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(tok_a, tok_b) and torch.equal(n_a, n_b) and torch.equal(len_a, len_b)
+    assert torch.allclose(conf_a, conf_b, rtol=1e-5, atol=0)
+    assert torch.equal(kc_a, kc_b) and torch.equal(vc_a, vc_b)
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     """batch * B * ceil(V / 8192) above 65536 is refused before anything is launched."""
     f = _lib.lib().mars_accept_noalloc

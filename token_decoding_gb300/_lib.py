@@ -23,6 +23,7 @@ MARS_ERR_WORKSPACE_TOO_SMALL = 2
 MARS_ERR_CUDA = 3
 MARS_ERR_UNSUPPORTED_DEVICE = 4
 MARS_ERR_SCRATCH_LIMIT = 5
+MARS_ERR_SCRATCH_NOT_READY = 6
 
 MARS_ACCEPT_MARGIN = 1
 MARS_ACCEPT_BATCH_MIN = 2
@@ -51,6 +52,7 @@ _SIGNATURES = {
     "mars_accept_margin": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_ex": (_I, [_P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_noalloc": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "mars_selftest_wait_timeout": (_I, [_I, ctypes.c_uint, _P, _P, _P]),
 }
 
 _lib = None
@@ -366,3 +368,14 @@ def accept_noalloc(logits, tau: float, k_new, v_new, k_cache, v_cache, cache_len
           _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit), _ptr(status),
           _stream(stream))
     return tokens, conf, n_commit
+
+
+def selftest_wait_timeout(withhold: bool, spin_limit: int, status, elapsed_ns=None, stream=None):
+    """Run the library's bounded pipeline wait on the device (include/mars.h:
+    mars_selftest_wait_timeout).  status: int32 [1] CUDA tensor (MARS_DEV_TIMEOUT is
+    OR-ed in when the wait gives up); elapsed_ns: optional int64 [1] CUDA tensor."""
+    _check(status, "status", torch.int32, (1,))
+    if elapsed_ns is not None:
+        _check(elapsed_ns, "elapsed_ns", torch.int64, (1,), status.device)
+    _call("mars_selftest_wait_timeout", 1 if withhold else 0, int(spin_limit), _ptr(status), _ptr(elapsed_ns),
+          _stream(stream))

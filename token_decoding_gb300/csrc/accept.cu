@@ -26,6 +26,7 @@
 //     one row's partials and writes tokens / conf, a ballot over the B
 //     confidences gives the commit count, and the committed K/V rows are
 //     copied into the cache.
+#include <cuda.h>
 #include <math.h>
 
 #include <algorithm>
@@ -642,24 +643,66 @@ constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_accept_scratch[kNoAllocScratchBytes];
 
-void* g_noalloc_scratch[kNoAllocMaxDevices];
+// The array's device address, resolved once per (device, CUDA context): a new
+// context on the same device (after cudaDeviceReset, say) reloads the module,
+// possibly at another address, so the cache is keyed on the context's id too.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+ScratchAddr g_noalloc_scratch[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
 
-// Device address of g_accept_scratch on the current device.  The first call on
-// a device resolves the address with that device current (in host code the
-// array's name is only a host-side stand-in, not a device address).
-int noalloc_scratch(char** out) {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current CUDA context (0 if it cannot be read).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_accept_scratch in the current device's context.  The first
+// call in a context resolves it with that device current (in host code the
+// array's name is only a host-side stand-in, not a device address).  That look-up
+// is not a stream operation, so it is refused while `stream` is being captured.
+int noalloc_scratch(cudaStream_t stream, char** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MARS_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return MARS_ERR_UNSUPPORTED_DEVICE;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_scratch[dev] == nullptr) {
+  ScratchAddr& slot = g_noalloc_scratch[dev];
+  if (slot.ptr == nullptr || slot.ctx_id != ctx || ctx == 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+    if (ce != cudaSuccess) return mars_host::cuda_fail(ce);
+    if (cs != cudaStreamCaptureStatusNone) return MARS_ERR_SCRATCH_NOT_READY;
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
     if (e != cudaSuccess || p == nullptr) return mars_host::cuda_fail(e);
-    g_noalloc_scratch[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = ctx;
   }
-  *out = static_cast<char*>(g_noalloc_scratch[dev]);
+  *out = static_cast<char*>(slot.ptr);
   return MARS_OK;
 }
 
@@ -669,16 +712,15 @@ extern "C" int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int
                                    const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
                                    uint16_t* v_cache, int32_t* cache_len, int Hkv, int D, int cap, int32_t* tokens,
                                    float* conf, int32_t* n_commit, int32_t* status, void* stream) {
-  MARS_HOST_CHECK(batch > 0 && B > 0 && V > 0, MARS_ERR_INVALID_ARG);
-  MARS_HOST_CHECK(static_cast<long long>(batch) * B * chunks_for(V) <= static_cast<long long>(kNoAllocPartialSlots),
-                  MARS_ERR_SCRATCH_LIMIT);
   int rc = check_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
                       conf, n_commit, status);
   if (rc != MARS_OK) return rc;
+  MARS_HOST_CHECK(static_cast<long long>(batch) * B * chunks_for(V) <= static_cast<long long>(kNoAllocPartialSlots),
+                  MARS_ERR_SCRATCH_LIMIT);
   rc = mars_host::check_device();
   if (rc != MARS_OK) return rc;
   char* scratch = nullptr;
-  rc = noalloc_scratch(&scratch);
+  rc = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
   if (rc != MARS_OK) return rc;
 
   AcceptArgs a = make_args(logits, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,

@@ -66,6 +66,9 @@ extern "C" const char* mars_status_string(int status) {
       return "the current device is not compute capability 10.3 (GB300, sm_103a)";
     case MARS_ERR_SCRATCH_LIMIT:
       return "shape exceeds the fixed scratch of mars_accept_noalloc (batch * B * ceil(V / 8192) <= 65536)";
+    case MARS_ERR_SCRATCH_NOT_READY:
+      return "mars_accept_noalloc's scratch is not set up in this CUDA context yet and the stream is being "
+             "captured: make one call outside capture first";
     default:
       return "unknown status";
   }

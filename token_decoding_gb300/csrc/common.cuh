@@ -3,7 +3,7 @@
 // Thin inline-PTX wrappers for the pieces the kernels use: cp.async, ldmatrix,
 // mma.sync (bf16), mbarrier, TMA (cp.async.bulk.tensor), tcgen05 (TMEM alloc,
 // MMA, commit, ld/st) and cluster distributed shared memory.  Every wait on an
-// mbarrier is bounded: after MARS_SPIN_LIMIT polls it gives up, and the caller
+// mbarrier is bounded: after kSpinLimit polls it gives up, and the caller
 // records MARS_DEV_TIMEOUT instead of hanging the GPU.
 #pragma once
 
@@ -143,21 +143,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded busy-poll (never suspends the thread): for a single issuing thread
-// that must react to a completion as soon as it happens.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  for (uint32_t i = 0; i < 64u * kSpinLimit; ++i) {
-    if (mbar_test_wait(a, parity)) return true;
-  }
-  return false;
-}
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (and leaves the barrier alone) when the poll limit is reached.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// (and leaves the barrier alone) when `limit` polls have found it incomplete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kSpinLimit) {
   const uint32_t a = smem_u32(bar);
   if (mbar_test_wait(a, parity)) return true;  // already complete: no suspend
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(a, parity)) return true;
   }
   return false;
