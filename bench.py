@@ -284,9 +284,9 @@ class DecodeWork:
         st = self.sets[step % self.nsets]
         mars.decode_attn(self.q, self.kn, self.vn, st["kc"], st["vc"], st["lens"], self.max_len, o=self.o)
 
-    def run_accept(self, mars, step, n_out, gate="prob"):
+    def run_accept(self, mars, step, n_out, gate="prob", tau=DECODE_TAU):
         st = self.sets[step % self.nsets]
-        mars.accept(st["logits"], DECODE_TAU, self.kn, self.vn, st["kc"], st["vc"], st["lens"], workspace=st["ws"],
+        mars.accept(st["logits"], tau, self.kn, self.vn, st["kc"], st["vc"], st["lens"], workspace=st["ws"],
                     tokens=self.tokens, conf=self.conf, n_commit=n_out, gate=gate)
 
     def byte_counts(self, records):
@@ -382,7 +382,6 @@ def run_gpu(args, rank, world, local):
         step(args.warmup + k, events[k])
     t_end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop((win0, datetime.datetime.now()))
     barrier(dist, world)
     total_ms = t_start.elapsed_time(t_end)
     per_kernel_ms = {n: [events[k][j].elapsed_time(events[k][j + 1]) for k in range(args.steps)]
@@ -462,6 +461,18 @@ def run_gpu(args, rank, world, local):
     if not args.no_graph:
         parts["decode_step_b1"].update(run_graph(mars, dec1, device, peaks["hbm_gbs"]))
         parts["decode_step_b64"].update(run_graph(mars, dec64, device, peaks["hbm_gbs"]))
+        # the batch-1 workload's four thresholds, each a 256-step episode in one graph
+        parts["decode_step_b1"]["tau_sweep"] = {
+            str(tau): run_graph(mars, dec1, device, peaks["hbm_gbs"], tau=tau) for tau in dec1.s.taus}
+        # Batch-1 kernels are shorter than a host launch, so the in-step event times
+        # above include host gaps: their roofline comes from 256 launches of the one
+        # kernel captured in a graph (rotating buffer sets), device time per launch.
+        for n, kind in (("decode_attn_b1", "decode"), ("accept_b1", "accept")):
+            us, byts = run_graph_kernel(mars, dec1, kind)
+            parts[n] = {"avg_us": round(us, 3), "timing": "256 launches in one CUDA graph",
+                        "in_step_event_avg_us": parts[n]["avg_us"],
+                        "roofline": roofline("hbm", byts / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s",
+                                             traffic.get(n))}
     # variants of the accept row, timed on their own after the step loop: the margin
     # gate and the batch-minimum cache mode (the paper's original sampler)
     parts["accept_margin_b64"] = run_accept_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic,
@@ -474,6 +485,10 @@ def run_gpu(args, rank, world, local):
     # the backward of the training-mask attention on both training shapes
     parts["train_bwd_05b"] = run_train_bwd(args, mars, train05, peaks["bf16_tflops"], traffic, "train_bwd_05b")
     parts["train_bwd_7b"] = run_train_bwd(args, mars, train7, peaks["bf16_tflops"], traffic, "train_bwd_7b")
+
+    # the clock record spans every timed phase above (step loop, back-to-back
+    # training launches, e2e, graph episodes, variants, backward)
+    clk = clocks.stop((win0, datetime.datetime.now()))
 
     line = {
         "metric": METRIC,
@@ -498,6 +513,8 @@ def run_gpu(args, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        for name, cb in cpu_baselines_per_part(args.cpu_seconds).items():
+            parts[name]["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -710,10 +727,10 @@ def run_train_bwd(args, mars, work, peak, traffic, name):
             "roofline": roofline("tensor", achieved, peak, "TFLOP/s", traffic.get(name))}
 
 
-def run_graph(mars, work, device, hbm_peak):
+def run_graph(mars, work, device, hbm_peak, tau=DECODE_TAU):
     """A whole decode episode (decode attention + accept per step: 256 steps at batch 1,
-    128 at batch 64) captured as one CUDA graph; device-side steps/s and the
-    algorithmic GB/s of the episode."""
+    128 at batch 64) captured as one CUDA graph; device-side steps/s, tokens per
+    step and the algorithmic GB/s of the episode."""
     import torch
 
     n_steps = work.s.steps
@@ -723,13 +740,13 @@ def run_graph(mars, work, device, hbm_peak):
         work.reset()
         for i in range(2):
             work.run_decode(mars, i)
-            work.run_accept(mars, i, n_out[i])
+            work.run_accept(mars, i, n_out[i], tau=tau)
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(n_steps):
                 work.run_decode(mars, i)
-                work.run_accept(mars, i, n_out[i])
+                work.run_accept(mars, i, n_out[i], tau=tau)
         reps = 3
         work.reset()
         graph.replay()
@@ -750,37 +767,127 @@ def run_graph(mars, work, device, hbm_peak):
     work.reset()
     gbs = reps * (sum(dec_b) + sum(acc_b)) / (ms * 1e-3) / 1e9
     return {"graph_steps_per_s": round(reps * n_steps / (ms * 1e-3), 1), "graph_GB_per_s": round(gbs, 1),
-            "graph_frac_of_hbm": round(gbs / hbm_peak, 4)}
+            "graph_frac_of_hbm": round(gbs / hbm_peak, 4), "graph_us_per_step": round(ms * 1e3 / (reps * n_steps), 3),
+            "tokens_per_step": round(float(hist.sum(axis=1).mean()), 3)}
+
+
+def run_graph_kernel(mars, work, kind, n_launches=256, reps=3):
+    """n_launches of one kernel (decode attention, or accept + append) over the
+    rotating buffer sets, captured in one CUDA graph; returns (device us per launch,
+    algorithmic bytes per launch)."""
+    import torch
+
+    s = work.s
+    stream = torch.cuda.Stream(device=work.q.device)
+    n_out = torch.zeros((n_launches, s.batch), dtype=torch.int32, device=work.q.device)
+
+    def body():
+        for i in range(n_launches):
+            if kind == "decode":
+                work.run_decode(mars, i)
+            else:
+                work.run_accept(mars, i, n_out[i])
+
+    with torch.cuda.stream(stream):
+        work.reset()
+        body()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            body()
+        ms = 0.0
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for _ in range(reps + 1):
+            work.reset()
+            stream.synchronize()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            stream.synchronize()
+            ms_rep = e0.elapsed_time(e1)
+            if _ > 0:  # the first replay warms up
+                ms += ms_rep
+    hist = n_out.cpu().numpy()
+    work.reset()
+    kv_row = s.Hkv * s.D * 2 * 2
+    small = s.batch * s.B * (2 * s.Hkv + 2 * s.Hq) * s.D * 2
+    if kind == "decode":
+        byts = int(work.lens0_host.sum()) * kv_row + small  # decode reads the reset lengths every launch
+    else:
+        byts = s.batch * s.B * s.V * 2 + float(hist.sum(axis=1).mean()) * 2 * kv_row + s.batch * s.B * 8 + s.batch * 8
+    return ms * 1e3 / (reps * n_launches), byts
 
 
 # --------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline and the reference arm)
 # --------------------------------------------------------------------------
 
-def oracle_train_sample(budget_s):
-    """Time the fp64 oracle on whole (batch, head) slices of the 0.5B-shaped
-    training batch until about budget_s seconds have passed; returns
+def oracle_train_sample(budget_s, shape=None):
+    """Time the fp64 oracle on whole (batch, head) slices of a training batch (the
+    0.5B-shaped one by default) until about budget_s seconds have passed; returns
     (useful TFLOP/s, description, seconds)."""
     import oracle
     from token_decoding_gb300 import synth
 
-    s = synth.TRAIN_05B
+    s = synth.TRAIN_05B if shape is None else shape
     q, k, v = synth.train_inputs(s)
     per_head = 4 * s.D * s.L * (s.L + 1)
     done = 0
-    t0 = time.perf_counter()
+    el = 0.0
     heads = 0
     while True:
         b, h = divmod(heads % (s.batch * s.Hq), s.Hq)
         g = h // (s.Hq // s.Hkv)
+        t0 = time.perf_counter()
         oracle.train_attn(q.f64[b:b + 1, :, h:h + 1], k.f64[b:b + 1, :, g:g + 1], v.f64[b:b + 1, :, g:g + 1],
                           s.L, s.B, s.D ** -0.5)
+        el += time.perf_counter() - t0
         done += per_head
         heads += 1
-        el = time.perf_counter() - t0
         if el >= budget_s:
             break
     return done / el / 1e12, f"{heads} (batch, head) slices of {s.name}, fp64 numpy, dense 2L x 2L masked", el
+
+
+def oracle_decode_sample(budget_s, shape, tau=DECODE_TAU):
+    """Time the fp64 oracle's sliding-window step (decode attention, acceptance,
+    KV append) on the decode workload `shape` until about budget_s seconds of
+    oracle time have passed.  Sequences are independent, so the sample is whole
+    steps of single sequences (in index order, up to 8 steps each from its own
+    initial cache length, so the sample spreads over the batch's lengths); the
+    batch's steps/s is one over (mean time per sequence-step x batch).
+    Input drawing is not timed.  Returns (steps/s, description, seconds)."""
+    import oracle
+    from token_decoding_gb300 import synth
+
+    s = shape
+    lens0 = synth.initial_cache_lens(s)
+    el = 0.0
+    seq_steps = 0
+    seqs = 0
+    scale = s.D ** -0.5
+    per_seq = s.steps if s.batch == 1 else min(s.steps, 8)  # spread the sample over the batch's lengths
+    while el < budget_s and seqs < s.batch:
+        b = seqs
+        kc, vc = synth.seq_cache_inputs(s, b, int(lens0[b]))
+        kc64, vc64, lens = kc.f64, vc.f64, np.array([lens0[b]], dtype=np.int64)
+        for t in range(per_seq):
+            q, kn, vn = synth.seq_step_inputs(s, t, b)
+            logits = synth.seq_step_logits(s, t, b)
+            t0 = time.perf_counter()
+            oracle.decode_attn(q.f64, kn.f64, vn.f64, kc64, vc64, lens, scale)
+            _, _, n = oracle.accept(logits.f64, tau)
+            kc64, vc64, lens = oracle.append_kv(kc64, vc64, lens, kn.f64, vn.f64, n)
+            el += time.perf_counter() - t0
+            seq_steps += 1
+            if el >= budget_s:
+                break
+        seqs += 1
+    per_seq_step = el / seq_steps
+    desc = (f"{seq_steps} sequence-steps of {s.name} over {seqs} sequence(s) (oracle decode_attn + accept + "
+            f"append_kv, tau {tau}), scaled to the batch of {s.batch}")
+    return 1.0 / (per_seq_step * s.batch), desc, el
 
 
 def cpu_cores():
@@ -796,6 +903,22 @@ def cpu_baseline(budget_s):
             "sample": sample + " (numpy BLAS threads: all available cores)"}
 
 
+def cpu_baselines_per_part(budget_s):
+    """The oracle beside every timed configuration: the 7B-shaped training batch
+    (TFLOP/s) and both decode workloads (steps/s)."""
+    from token_decoding_gb300 import synth
+
+    out = {}
+    val, sample, _ = oracle_train_sample(budget_s, synth.TRAIN_7B)
+    out["train_7b"] = {"value": round(val, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                       "sample": sample}
+    for name, shape in (("decode_step_b1", synth.DECODE_7B_B1), ("decode_step_b64", synth.DECODE_7B_B64)):
+        val, sample, _ = oracle_decode_sample(budget_s, shape)
+        out[name] = {"value": round(val, 4), "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+                     "sample": sample}
+    return out
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -809,6 +932,10 @@ def run_reference(args, rank, world):
         vals.append(v)
         secs += el
     value = float(np.mean(vals)) if vals else 0.0
+    # the clock record spans every timed phase above (step loop, back-to-back
+    # training launches, e2e, graph episodes, variants, backward)
+    clk = clocks.stop((win0, datetime.datetime.now()))
+
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(secs / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
