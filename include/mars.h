@@ -146,6 +146,14 @@ int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * A cache_len outside [0, max_len] sets MARS_DEV_LEN_RANGE and that
  * sequence's output is written as zeros.  No workspace.
  */
+/*
+ * mars_decode_attn_workspace_size - bytes of workspace mars_decode_attn needs,
+ * which is always 0 (it takes none).  The splits of one unit's cache are merged
+ * inside its thread-block cluster through distributed shared memory, so no
+ * partial result goes through global memory.  The query exists for callers
+ * written against a split-K decode call that asks for its workspace first.
+ */
+size_t mars_decode_attn_workspace_size(int batch, int B, int Hq, int D, int max_len);
 int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                      const uint16_t* k_cache, const uint16_t* v_cache,
                      const int32_t* cache_len,
@@ -210,13 +218,17 @@ int mars_decode_attn_deferred(const uint16_t* q, const uint16_t* k_new, const ui
  *   cache_len        [batch] int32, device, in/out
  *   tokens [batch, B] int32, conf [batch, B] fp32, n_commit [batch] int32 (written)
  *   workspace        device buffer of >= mars_accept_workspace_size(batch, B, V)
- *                    bytes.  It holds one partial result per 16 KB slice of
- *                    logits (and, for the batch-minimum mode of mars_accept_ex,
- *                    one count per sequence); its contents on entry do not
- *                    matter.  Calls that share a workspace must not overlap in
- *                    time.
- * The call is two kernel launches on `stream` (the streaming reduction, then
- * one CTA per sequence for the commit rule and the append).
+ *                    bytes, ZERO-FILLED BEFORE ITS FIRST USE (cudaMemset,
+ *                    torch.zeros).  It holds one partial result per slice of
+ *                    logits (4 to 16 KB), one count per sequence (batch-minimum
+ *                    mode of mars_accept_ex) and one ticket per sequence; every
+ *                    call leaves the tickets at zero again, so a workspace is
+ *                    zeroed once and then reused.  Calls that share a workspace
+ *                    must not overlap in time.
+ * The call is one kernel launch on `stream`: persistent CTAs stream the logits
+ * in slices; the warp that reduces the last slice of a sequence (an atomic
+ * ticket per sequence, no waiting) applies the commit rule and appends.
+ * (The batch-minimum mode of mars_accept_ex adds two short launches.)
  * If cache_len[b] + n > cap nothing is appended for b, cache_len[b] is kept,
  * n_commit[b] is 0 and MARS_DEV_CAPACITY is set.
  * Supported: 1 <= B <= 16, 1 <= V, D % 8 == 0, D <= 256.
@@ -329,8 +341,8 @@ int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int V, float t
  *   withhold_arrival  nonzero: the second arrival never comes, so the wait
  *                     gives up after spin_limit polls; nothing asynchronous
  *                     (no copy, no tensor-core commit) targets the barrier
- *   spin_limit        polls before the wait gives up, 1 .. 2^24 (the kernels'
- *                     own limit is the maximum)
+ *   spin_limit        polls before the wait gives up, 1 .. 2^20 (the kernels'
+ *                     own limit, about 4 s on GB300, is the maximum)
  *   status           device int32 word: MARS_DEV_TIMEOUT is OR-ed in when the
  *                     wait gave up (required)
  *   elapsed_ns       device uint64 (8-byte aligned, may be NULL): nanoseconds

@@ -27,7 +27,7 @@ def lib():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "mars_accept", "mars_accept_ex", "mars_accept_margin", "mars_accept_noalloc", "mars_accept_workspace_size",
-        "mars_decode_attn", "mars_decode_attn_deferred", "mars_last_cuda_error", "mars_selftest_wait_timeout",
+        "mars_decode_attn", "mars_decode_attn_deferred", "mars_decode_attn_workspace_size", "mars_last_cuda_error", "mars_selftest_wait_timeout",
         "mars_train_attn_bwd", "mars_train_attn_bwd_workspace_size", "mars_status_string", "mars_train_attn", "mars_version"])
 
 
@@ -45,6 +45,8 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_size_is_host_only(lib):
+    lib.mars_decode_attn_workspace_size.restype = ctypes.c_size_t
+    assert lib.mars_decode_attn_workspace_size(64, 8, 28, 128, 4096) == 0  # the merge never leaves the cluster
     lib.mars_accept_workspace_size.restype = ctypes.c_size_t
     assert lib.mars_accept_workspace_size(0, 4, 10) == 0
     n = lib.mars_accept_workspace_size(64, 8, 152064)

@@ -45,6 +45,7 @@ _SIGNATURES = {
     "mars_train_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "mars_train_attn_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "mars_train_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+    "mars_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "mars_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_decode_attn_deferred": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
     "mars_accept_workspace_size": (_SZ, [_I, _I, _I]),
@@ -200,6 +201,11 @@ def train_attn_bwd(q, k, v, o, dout, lse, L: int, B: int, scale: float | None = 
           _ptr(dv), nb, L, B, hq, hkv, d, float(scale), _ptr(workspace), workspace.numel(), _ptr(status),
           _stream(stream))
     return dq, dk, dv
+
+
+def decode_attn_workspace_size(batch: int, B: int, Hq: int, D: int, max_len: int) -> int:
+    """Workspace bytes of decode_attn (include/mars.h: always 0, the merge stays in the cluster)."""
+    return int(_fn("mars_decode_attn_workspace_size")(batch, B, Hq, D, max_len))
 
 
 def decode_attn(q, k_new, v_new, k_cache, v_cache, cache_len, max_len: int, scale: float | None = None, o=None,

@@ -21,9 +21,11 @@
 namespace mars {
 
 constexpr float kLog2e = 1.4426950408889634f;
-// try_wait polls before a wait is declared dead (each poll may suspend the
-// thread for a short, hardware-chosen time; this is far beyond any real wait).
-constexpr uint32_t kSpinLimit = 1u << 24;
+// try_wait polls before a wait is declared dead.  Each poll may suspend the
+// thread for a short, hardware-chosen time (measured on GB300: ~3.8 us per
+// failing poll), so 2^20 polls give up after ~4 s of running time, far beyond
+// any real wait inside these kernels (the longest run well under 1 ms).
+constexpr uint32_t kSpinLimit = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -302,6 +304,23 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
   return r;
+}
+// Split cluster barrier: arrive (relaxed: orders nothing) now, wait later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+// Arrive, releasing this thread's earlier writes (shared::cluster stores included) to the cluster.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+// Wait for the current cluster barrier phase, acquiring the writes the arrivals released.
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st_f32x4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
   float v;

@@ -72,7 +72,12 @@ struct DCfg {
   static constexpr int NV_OFF = NK_OFF + NB * N_BOX;
   static constexpr int RING_OFF = NV_OFF + NB * N_BOX;  // stage s: K boxes then V boxes
   static constexpr int STAGE = 2 * NB * T_BOX;
-  static constexpr int SMEM = RING_OFF + NS * STAGE + 1024;  // + slack to align the base to 1024
+  // Inbox of the small-unit cluster merge (units of <= 32 rows): one combined state
+  // per (owned row, source CTA): acc [slots][D] f32, then m [slots], l [slots].
+  static constexpr int IN_SLOTS = 32 + kMaxCluster - 1;  // >= ceil(R / C) * C for R <= 32
+  static constexpr int INBOX_OFF = RING_OFF + NS * STAGE;
+  static constexpr int INBOX_BYTES = IN_SLOTS * D * 4 + 2 * IN_SLOTS * 4;
+  static constexpr int SMEM = INBOX_OFF + INBOX_BYTES + 1024;  // + slack to align the base to 1024
   static constexpr int TMEM_COLS = D == 64 ? 256 : 512;       // S_A | S_B | O_A | O_B
   static constexpr int O_COL = 2 * kTileKeys;
   // end-of-kernel merge state (overlays the ring): acc [2][128][D] f32, m [2][128], l [2][128],
@@ -138,6 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int R = a.Gc * a.S;            // rows loaded (row = slot i * Gc + head)
   const int act_warps = (R + 31) / 32;  // softmax warps per stream with real rows
+  // Small units split over a cluster (R <= 32): Q is loaded twice, at rows 0 and 32,
+  // so stream B's rows live in tensor-memory lanes 32..63 and its softmax warp runs
+  // on another SM sub-partition than stream A's; the two streams are combined in
+  // the CTA and each row's C states are pushed into the CTA that finishes the row.
+  const bool dup = R <= 32 && a.C > 1;
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     mbar_init(&bar_new, 1);
@@ -152,6 +162,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  if (dup) cluster_arrive_relaxed();  // matched by the wait before the first push into a peer
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_kn);
+    tma_prefetch_desc(&tm_vn);
+  }
+  const uint32_t q_s = smem_u32(smem + C::Q_OFF);
+  const uint32_t nk_s = smem_u32(smem + C::NK_OFF);
+  const uint32_t nv_s = smem_u32(smem + C::NV_OFF);
+  const uint32_t ring = smem_u32(smem + C::RING_OFF);
+  // Set-up that touches no global memory runs before the wait below, beside the
+  // tail of the previous kernel: zero the rows the TMA loads never write (Q rows
+  // >= R, new-key rows >= S: the tail of every Q box and of every new-key box) and
+  // allocate tensor memory.
+  {
+    const int q_hi = dup ? 32 : kRows;  // zero Q rows [R, q_hi) and, with dup, [32 + R, 128)
+    for (int bx = 0; bx < C::NB; ++bx) {
+      for (int e = tid; e < (q_hi - R) * 8; e += kThreads) st_shared_v4(q_s + bx * C::Q_BOX + R * 128 + e * 16, 0u, 0u, 0u, 0u);
+      if (dup)
+        for (int e = tid; e < (kRows - 32 - R) * 8; e += kThreads)
+          st_shared_v4(q_s + bx * C::Q_BOX + (32 + R) * 128 + e * 16, 0u, 0u, 0u, 0u);
+    }
+  }
+  for (int bx = 0; bx < 2 * C::NB; ++bx)  // new K boxes, then new V boxes
+    for (int e = tid; e < (kNewKeys - a.S) * 8; e += kThreads)
+      st_shared_v4(nk_s + bx * C::N_BOX + a.S * 128 + e * 16, 0u, 0u, 0u, 0u);
+  fence_async_smem();
+  if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
   // launched as a programmatic dependent: nothing global is read before the previous
   // kernel in the stream has completed
   griddep_wait();
@@ -199,6 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(0, 0, 0, 0);
       }
     }
+    __syncthreads();  // tensor memory was allocated before the wait: free it (no product was issued)
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_slot, C::TMEM_COLS);
+    }
     return;
   }
   // slot validity bitmask: every slot, or (deferred) the pending slots below pend and all placeholders
@@ -210,10 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool has_new = crank == a.C - 1;
   const int ntiles = ncache + (has_new ? 1 : 0);  // local tile k: cache tile t0 + k, then the new tile
 
-  const uint32_t q_s = smem_u32(smem + C::Q_OFF);
-  const uint32_t nk_s = smem_u32(smem + C::NK_OFF);
-  const uint32_t nv_s = smem_u32(smem + C::NV_OFF);
-  const uint32_t ring = smem_u32(smem + C::RING_OFF);
   const uint32_t tile_bytes = C::NB * 128 * a.box_rows;
   // TMA loads of cache tile k into its ring stage (the stage is free)
   auto load_tile = [&](int k) {
@@ -226,13 +268,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(vb + c * C::T_BOX, &tm_vc, &bar_kv[st], 64 * c, key0, g, b);
     }
   };
-  // The producer thread starts the loads before the rest of the set-up: they write
-  // rows the zeroing below never touches.
-  if (tid == 0 && ntiles > 0) {
-    mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R);
-    for (int c = 0; c < C::NB; ++c) tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
-    for (int k = 0; k < min(ncache, C::NS); ++k) load_tile(k);
-    if (has_new) {
+  // The loads write rows the zeroing above never touched.  The lanes of warp 0
+  // issue them side by side: lane 0 the Q tile, lane 1 + k the first ring stages'
+  // cache tile k, lane NS + 1 the new-key tile (each has its own barrier).
+  if (warp == 0 && ntiles > 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R * (dup ? 2 : 1));
+      for (int c = 0; c < C::NB; ++c) {
+        tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
+        if (dup) tma_load_4d(q_s + c * C::Q_BOX + 32 * 128, &tm_q, &bar_q, 64 * c, h0, 0, b);
+      }
+    } else if (lane <= min(ncache, C::NS)) {
+      load_tile(lane - 1);
+    } else if (lane == C::NS + 1 && has_new) {
       mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.S);
       for (int c = 0; c < C::NB; ++c) {
         tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, b);
@@ -241,20 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- zero the rows the TMA loads never write (Q rows >= R, new-key rows >= S):
-  // the tail of every Q box and of every new-key box
-  for (int bx = 0; bx < C::NB; ++bx)
-    for (int e = tid; e < (kRows - R) * 8; e += kThreads) st_shared_v4(q_s + bx * C::Q_BOX + R * 128 + e * 16, 0u, 0u, 0u, 0u);
-  for (int bx = 0; bx < 2 * C::NB; ++bx)  // new K boxes, then new V boxes
-    for (int e = tid; e < (kNewKeys - a.S) * 8; e += kThreads)
-      st_shared_v4(nk_s + bx * C::N_BOX + a.S * 128 + e * 16, 0u, 0u, 0u, 0u);
-  fence_async_smem();
-  if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
-  tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   bool ok = true;
+  // small-unit merge (dup): this thread's half row after combining streams A and B
+  bool push = false;
+  int push_row = 0, push_half = 0;
+  float pc[D / 2];
+  float pc_m = -INFINITY, pc_l = 0.f;
 
   if (warp == 0) {
     // ================= TMA producer: the tiles past the first NS, each into a freed stage
@@ -362,8 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= softmax of stream x (warps 2..5: A, 6..9: B)
     const int x = (warp - 2) >> 2;
     const int quad = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = quad * 32 + lane;
-    const bool active = quad < act_warps;
+    const int qbase = (dup && x == 1) ? 1 : 0;  // first lane quarter holding this stream's rows
+    const int r = (quad - qbase) * 32 + lane;   // query row (rows >= R are padding)
+    const bool active = quad >= qbase && quad - qbase < act_warps;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_col = tmem + lane_addr + x * kTileKeys;
     const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
@@ -442,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_new, 0));
           if (!ok) break;
           const int per_box = (a.B - pend) * 8;  // 16-byte chunks of rows pend .. B-1
-          for (int e = quad * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
+          for (int e = (quad - qbase) * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
             const int bx = e / per_box, w = e % per_box;
             st_shared_v4(nv_s + bx * C::N_BOX + pend * 128 + w * 16, 0u, 0u, 0u, 0u);
           }
@@ -457,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int z0 = len - key0;
           const int per_box = (kTileKeys - z0) * 8;  // 16-byte chunks
           const uint32_t vb = ring + st * C::STAGE + C::NB * C::T_BOX;
-          for (int e = quad * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
+          for (int e = (quad - qbase) * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
             const int bx = e / per_box, w = e % per_box;
             st_shared_v4(vb + bx * C::T_BOX + z0 * 128 + w * 16, 0u, 0u, 0u, 0u);
           }
@@ -519,6 +563,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    } else if (dup) {
+      // ---- small unit over a cluster: combine streams A and B of each row in this
+      // CTA (through shared memory: their rows sit in different lane quarters), each
+      // thread keeping half of the row's columns for the push after this branch.
+      named_bar_sync(1, 256);  // both streams' products are complete: the ring is free
+      tc_fence_after();
+      float* xo = reinterpret_cast<float*>(smem + C::RING_OFF);  // [2][32][D], 16-byte units XOR (row & 7)
+      float* xm = xo + 2 * 32 * D;                               // [2][32]
+      float* xl = xm + 2 * 32;                                   // [2][32]
+      if (active) {
+        float4* dst = reinterpret_cast<float4*>(xo + (x * 32 + r) * D);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(o_col + c, ov);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                                __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[((c >> 2) + e) ^ (r & 7)] = v;
+          }
+        }
+        xm[x * 32 + r] = have ? m_used : -INFINITY;
+        xl[x * 32 + r] = have ? l : 0.f;
+      }
+      named_bar_sync(1, 256);
+      if (active && r < R) {
+        const float ma = xm[r], mb = xm[32 + r];
+        const float mx = fmaxf(ma, mb);
+        const float wa = ma == -INFINITY ? 0.f : fast_exp2(ma - mx);
+        const float wb = mb == -INFINITY ? 0.f : fast_exp2(mb - mx);
+        pc_m = mx;
+        pc_l = wa * xl[r] + wb * xl[32 + r];
+        const float4* xa = reinterpret_cast<const float4*>(xo + r * D);         // rows without tiles are zero
+        const float4* xb = reinterpret_cast<const float4*>(xo + (32 + r) * D);
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) {
+          const int c4 = x * (D / 8) + j;
+          const float4 va = xa[c4 ^ (r & 7)], vb = xb[c4 ^ (r & 7)];
+          pc[4 * j] = wa * va.x + wb * vb.x;
+          pc[4 * j + 1] = wa * va.y + wb * vb.y;
+          pc[4 * j + 2] = wa * va.z + wb * vb.z;
+          pc[4 * j + 3] = wa * va.w + wb * vb.w;
+        }
+        push = true;
+        push_row = r;
+        push_half = x;
+      }
     } else {
       // Both streams' products are complete once every softmax warp is past its
       // wait above, so the ring (every loaded tile consumed) can hold the merge state.
@@ -552,7 +646,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This CTA finishes rows [r_lo, r_hi): first one weight per (row, state),
   // w = 2^(m - max m) / sum_states(2^(m - max m) l), then O = sum w acc.
   tc_fence_before();
-  if (a.C > 1) {
+  if (dup) {
+    // Push: each row's combined state goes into the inbox of the CTA that finishes
+    // the row (rows [crank * rows_per, ...) belong to CTA crank), slot
+    // (row - first owned row) * C + source CTA; 16-byte units XOR (slot & 7).
+    const int rows_per = (R + a.C - 1) / a.C;
+    const uint32_t in_acc = smem_u32(smem + C::INBOX_OFF);
+    const uint32_t in_m = in_acc + C::IN_SLOTS * D * 4, in_l = in_m + C::IN_SLOTS * 4;
+    cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
+    if (push) {
+      const int owner = push_row / rows_per;
+      const int slot = (push_row - owner * rows_per) * a.C + crank;
+      const uint32_t row_l = in_acc + slot * D * 4;  // the slot's address in this CTA's window
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        const int c4 = push_half * (D / 8) + j;
+        dsmem_st_f32x4(dsmem_map(row_l + 16 * (c4 ^ (slot & 7)), owner), pc[4 * j], pc[4 * j + 1], pc[4 * j + 2],
+                       pc[4 * j + 3]);
+      }
+      if (push_half == 0) {
+        dsmem_st_f32(dsmem_map(in_m + 4 * slot, owner), pc_m);
+        dsmem_st_f32(dsmem_map(in_l + 4 * slot, owner), pc_l);
+      }
+    }
+    cluster_arrive_release();
+    cluster_wait();  // every push into this CTA's inbox has landed
+    // Finish the owned rows from local shared memory: one weight per (row, source),
+    // w = 2^(m - max m) / sum(2^(m - max m) l), then O = sum w acc.
+    const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
+    const int nrow = max(0, r_hi - r_lo);
+    float* w_s = reinterpret_cast<float*>(smem + C::RING_OFF);  // [rows_per][C] (the ring is free)
+    const float* acc_in = reinterpret_cast<const float*>(smem + C::INBOX_OFF);
+    const float* m_in = acc_in + C::IN_SLOTS * D;
+    const float* l_in = m_in + C::IN_SLOTS;
+    for (int t0 = 0; t0 < nrow * a.C; t0 += kThreads) {  // uniform trip count: every lane shuffles
+      const int t = t0 + tid;
+      const bool valid = t < nrow * a.C;
+      const float m = valid ? m_in[t] : -INFINITY, l = valid ? l_in[t] : 0.f;  // slot t = (row, source)
+      float mmax = m;
+      for (int o = a.C >> 1; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+      const float w = m == -INFINITY ? 0.f : fast_exp2(m - mmax);
+      float lsum = w * l;
+      for (int o = a.C >> 1; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      if (valid) w_s[t] = lsum > 0.f ? w / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
+    }
+    __syncthreads();
+    for (int e = tid; e < nrow * (D / 4); e += kThreads) {
+      const int rr = e / (D / 4), d4 = e % (D / 4);
+      const int r = r_lo + rr;
+      const int i = r / a.Gc, hl = r % a.Gc;
+      if (hl >= heads) continue;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < a.C; ++c) {
+        const int slot = rr * a.C + c;
+        const float w = w_s[slot];
+        const float4 v = reinterpret_cast<const float4*>(acc_in + slot * D)[d4 ^ (slot & 7)];
+        o.x += w * v.x;
+        o.y += w * v.y;
+        o.z += w * v.z;
+        o.w += w * v.w;
+      }
+      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+    }
+    __syncthreads();  // every tensor-memory read of the epilogue is done
+  } else if (a.C > 1) {
     cluster_sync();
     {
       const float* acc_s = reinterpret_cast<const float*>(smem + C::RING_OFF);
@@ -562,30 +720,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc_l = smem_u32(acc_s), m_l = smem_u32(m_s), l_l = smem_u32(l_s);
       const int rows_per = (R + a.C - 1) / a.C;
       const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
-      const int ns = 2 * a.C;  // states per row
-      for (int r = r_lo + tid; r < r_hi; r += kThreads) {
-        float m[2 * kMaxCluster], l[2 * kMaxCluster];
-        float mmax = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 2 * kMaxCluster; ++q) {
-          if (q < ns) {
-            m[q] = dsmem_ld_f32(dsmem_map(m_l + 4 * ((q & 1) * kRows + r), q >> 1));
-            l[q] = dsmem_ld_f32(dsmem_map(l_l + 4 * ((q & 1) * kRows + r), q >> 1));
-            mmax = fmaxf(mmax, m[q]);
-          }
+      const int ns = 2 * a.C;  // states per row: a power of two <= 16, so a row's states are aligned lanes
+      // One thread per (row, state): every state's (m, l) is requested at once, then
+      // the row's max and weighted sum are reduced with shuffles among its ns lanes.
+      const int nrow = r_hi - r_lo;
+      for (int t0 = 0; t0 < nrow * ns; t0 += kThreads) {  // uniform trip count: every lane shuffles
+        const int t = t0 + tid;
+        const bool valid = t < nrow * ns;
+        const int r = r_lo + t / ns, q = t % ns;
+        float m = -INFINITY, l = 0.f;
+        if (valid) {
+          m = dsmem_ld_f32(dsmem_map(m_l + 4 * ((q & 1) * kRows + r), q >> 1));
+          l = dsmem_ld_f32(dsmem_map(l_l + 4 * ((q & 1) * kRows + r), q >> 1));
         }
-        float lsum = 0.f;
-#pragma unroll
-        for (int q = 0; q < 2 * kMaxCluster; ++q) {
-          if (q < ns) {
-            m[q] = m[q] == -INFINITY ? 0.f : fast_exp2(m[q] - mmax);
-            lsum += m[q] * l[q];
-          }
-        }
+        float mmax = m;
+        for (int o = ns >> 1; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+        const float w = m == -INFINITY ? 0.f : fast_exp2(m - mmax);
+        float lsum = w * l;
+        for (int o = ns >> 1; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
-#pragma unroll
-        for (int q = 0; q < 2 * kMaxCluster; ++q)
-          if (q < ns) w_s[(r - r_lo) * 2 * kMaxCluster + q] = m[q] * inv;
+        if (valid) w_s[(r - r_lo) * 2 * kMaxCluster + q] = w * inv;
       }
       __syncthreads();
       for (int e = tid; e < (r_hi - r_lo) * (D / 4); e += kThreads) {
@@ -763,6 +917,8 @@ int decode_impl(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
 }
 
 }  // namespace
+
+extern "C" size_t mars_decode_attn_workspace_size(int, int, int, int, int) { return 0; }
 
 extern "C" int mars_decode_attn(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                                 const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* cache_len, int batch,
