@@ -195,6 +195,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Shared -> shared copy into another CTA of the cluster: `dst` and `bar` are
+// shared::cluster addresses in that CTA (from dsmem_map), `src` this CTA's; the
+// bytes complete as transactions on that CTA's barrier (16-byte aligned, size a
+// multiple of 16).  Completion of the read of `src`: bulk_commit_group + bulk_wait_read_all.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Shared -> global tiled store (bulk-group completion).  Rows of the box that
 // fall outside the tensor are not written.
 __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1, int c2, int c3) {

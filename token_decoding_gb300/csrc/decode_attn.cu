@@ -72,11 +72,17 @@ struct DCfg {
   static constexpr int NV_OFF = NK_OFF + NB * N_BOX;
   static constexpr int RING_OFF = NV_OFF + NB * N_BOX;  // stage s: K boxes then V boxes
   static constexpr int STAGE = 2 * NB * T_BOX;
-  // Inbox of the small-unit cluster merge (units of <= 32 rows): one combined state
-  // per (owned row, source CTA): acc [slots][D] f32, then m [slots], l [slots].
+  // Small-unit cluster merge (units of <= 32 rows): a row's state travels as D + 4
+  // floats (acc[D], m, l, two pad), ROWB bytes.  The inbox holds one block per
+  // source CTA of the rows this CTA finishes: [C][rows_per][D + 4].
+  static constexpr int ROWB = (D + 4) * 4;
   static constexpr int IN_SLOTS = 32 + kMaxCluster - 1;  // >= ceil(R / C) * C for R <= 32
   static constexpr int INBOX_OFF = RING_OFF + NS * STAGE;
-  static constexpr int INBOX_BYTES = IN_SLOTS * D * 4 + 2 * IN_SLOTS * 4;
+  static constexpr int INBOX_BYTES = IN_SLOTS * ROWB;
+  // the in-CTA combine of the small-unit merge overlays the ring: 8 states x 32 rows
+  // of acc, their m and l, then the outbox [32][D + 4]
+  static constexpr int XCH_BYTES = 8 * 32 * D * 4 + 2 * 8 * 32 * 4 + 32 * ROWB;
+  static_assert(XCH_BYTES <= NS * STAGE, "small-unit combine must fit in the ring");
   static constexpr int SMEM = INBOX_OFF + INBOX_BYTES + 1024;  // + slack to align the base to 1024
   static constexpr int TMEM_COLS = D == 64 ? 256 : 512;       // S_A | S_B | O_A | O_B
   static constexpr int O_COL = 2 * kTileKeys;
@@ -130,7 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = DCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q, bar_new, bar_kv[C::NS], bar_kv_empty[C::NS], bar_s[2], bar_p[2], bar_o[2];
+  __shared__ __align__(8) uint64_t bar_q, bar_new, bar_kv[C::NS], bar_kv_empty[C::NS], bar_s[2], bar_p[2], bar_o[2],
+      bar_in;
+  __shared__ float s_wmerge[C::IN_SLOTS];  // small-unit merge weights, [rows_per][C]
   __shared__ uint32_t tmem_slot;
   __shared__ int s_b;
   __shared__ float s_mstate[2][kRows], s_lstate[2][kRows];  // single-CTA units: each stream's (m, l) per row
@@ -143,11 +151,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int R = a.Gc * a.S;            // rows loaded (row = slot i * Gc + head)
   const int act_warps = (R + 31) / 32;  // softmax warps per stream with real rows
-  // Small units split over a cluster (R <= 32): Q is loaded twice, at rows 0 and 32,
-  // so stream B's rows live in tensor-memory lanes 32..63 and its softmax warp runs
-  // on another SM sub-partition than stream A's; the two streams are combined in
-  // the CTA and each row's C states are pushed into the CTA that finishes the row.
-  const bool dup = R <= 32 && a.C > 1;
+  // Small units split over a cluster (R <= 32 rows): Q is loaded into all four
+  // tensor-memory lane quarters, so each stream's S tile is split four ways by keys
+  // among warps on the four SM sub-partitions (16 keys of each 64-key tile per
+  // warp).  A CTA combines its 8 states of a row (2 streams x 4 quarters) and sends
+  // each owning CTA its rows with one bulk copy into that CTA's inbox.
+  const bool split4 = R <= 32 && a.C > 1;
+  const int rows_per = (R + a.C - 1) / a.C;  // rows finished by each CTA of a small unit
+  const int nrow_own = max(0, min(R, (crank + 1) * rows_per) - crank * rows_per);
   if (tid == 0) {
     mbar_init(&bar_q, 1);
     mbar_init(&bar_new, 1);
@@ -157,12 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s[x], 1);
-      mbar_init(&bar_p[x], 32 * act_warps);
+      mbar_init(&bar_p[x], split4 ? 128 : 32 * act_warps);
       mbar_init(&bar_o[x], 1);
     }
+    mbar_init(&bar_in, 1);
     fence_mbar_init();
+    // small units: this CTA's inbox expects its rows from every CTA of the cluster
+    if (split4) mbar_arrive_expect_tx(&bar_in, static_cast<uint32_t>(a.C * nrow_own * C::ROWB));
   }
-  if (dup) cluster_arrive_relaxed();  // matched by the wait before the first push into a peer
+  // matched by the wait before the first bulk copy into a peer: by then every CTA of
+  // the cluster has started and armed its inbox
+  if (split4) cluster_arrive_relaxed();
   if (tid == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kc);
@@ -178,14 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tail of the previous kernel: zero the rows the TMA loads never write (Q rows
   // >= R, new-key rows >= S: the tail of every Q box and of every new-key box) and
   // allocate tensor memory.
-  {
-    const int q_hi = dup ? 32 : kRows;  // zero Q rows [R, q_hi) and, with dup, [32 + R, 128)
-    for (int bx = 0; bx < C::NB; ++bx) {
-      for (int e = tid; e < (q_hi - R) * 8; e += kThreads) st_shared_v4(q_s + bx * C::Q_BOX + R * 128 + e * 16, 0u, 0u, 0u, 0u);
-      if (dup)
-        for (int e = tid; e < (kRows - 32 - R) * 8; e += kThreads)
-          st_shared_v4(q_s + bx * C::Q_BOX + (32 + R) * 128 + e * 16, 0u, 0u, 0u, 0u);
-    }
+  if (split4) {  // zero rows [32 j + R, 32 j + 32) of each lane quarter j
+    for (int bx = 0; bx < C::NB; ++bx)
+      for (int e = tid; e < 4 * (32 - R) * 8; e += kThreads) {
+        const int j = e / ((32 - R) * 8), w = e % ((32 - R) * 8);
+        st_shared_v4(q_s + bx * C::Q_BOX + (32 * j + R) * 128 + w * 16, 0u, 0u, 0u, 0u);
+      }
+  } else {
+    for (int bx = 0; bx < C::NB; ++bx)
+      for (int e = tid; e < (kRows - R) * 8; e += kThreads) st_shared_v4(q_s + bx * C::Q_BOX + R * 128 + e * 16, 0u, 0u, 0u, 0u);
   }
   for (int bx = 0; bx < 2 * C::NB; ++bx)  // new K boxes, then new V boxes
     for (int e = tid; e < (kNewKeys - a.S) * 8; e += kThreads)
@@ -199,6 +216,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- which sequence: heavy-first rank order (stable by index) or plain order
   const int b_rank = unit_rank / units_per_b;
+  const int rem = unit_rank % units_per_b;
+  const int g = rem / a.nhc;
+  const int hc = rem % a.nhc;
+  const int h0 = g * a.G + hc * a.Gc;            // first query head of this unit
+  const int heads = min(a.Gc, a.G - hc * a.Gc);  // real heads in this unit
+  const bool has_new = crank == a.C - 1;
+  // CTA rank c of a unit takes the unit's cache tiles c, c + C, c + 2 C, ...: local
+  // tile k is global tile c + k C, which is known before cache_len is read.
+  const uint32_t tile_bytes = C::NB * 128 * a.box_rows;
+  auto load_tile = [&](int k, int bseq) {  // TMA loads of local cache tile k into its (free) ring stage
+    const int st = k % C::NS;
+    const int key0 = (crank + k * a.C) * kTileKeys;
+    const uint32_t kb = ring + st * C::STAGE, vb = kb + C::NB * C::T_BOX;
+    mbar_arrive_expect_tx(&bar_kv[st], 2 * tile_bytes);
+    for (int c = 0; c < C::NB; ++c) {
+      tma_load_4d(kb + c * C::T_BOX, &tm_kc, &bar_kv[st], 64 * c, key0, g, bseq);
+      tma_load_4d(vb + c * C::T_BOX, &tm_vc, &bar_kv[st], 64 * c, key0, g, bseq);
+    }
+  };
+  // The first loads, issued by the lanes of warp 0 side by side: lane 0 the Q tile,
+  // lane 1 + k the ring stage of local cache tile k, lane NS + 1 the new-key tile
+  // (each has its own barrier).  They write rows the zeroing above never touched.
+  auto first_loads = [&](int bseq, int ncache_first, bool with_q) {
+    if (warp != 0) return;
+    if (lane == 0 && with_q) {
+      mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R * (split4 ? 4 : 1));
+      for (int c = 0; c < C::NB; ++c)
+        for (int j = 0; j < (split4 ? 4 : 1); ++j)  // split4: a copy at rows 0, 32, 64, 96
+          tma_load_4d(q_s + c * C::Q_BOX + j * 32 * 128, &tm_q, &bar_q, 64 * c, h0, 0, bseq);
+    } else if (lane >= 1 && lane <= ncache_first) {
+      load_tile(lane - 1, bseq);
+    } else if (lane == C::NS + 1 && has_new) {
+      mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.S);
+      for (int c = 0; c < C::NB; ++c) {
+        tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, bseq);
+        tma_load_4d(nv_s + c * C::N_BOX, &tm_vn, &bar_new, 64 * c, g, 0, bseq);
+      }
+    }
+  };
+  // In plain order the sequence is known at once, so Q, the new-key tile and this
+  // rank's first NS cache tiles (those that start inside the cache's capacity) are
+  // requested before cache_len is read: the read's latency then overlaps the loads.
+  // Loaded tiles past cache_len are never used; they are waited for before exit.
+  int nspec = 0;
+  if (!a.sort_units) {
+    while (nspec < C::NS && (crank + nspec * a.C) * kTileKeys < a.cap) ++nspec;
+    first_loads(b_rank, nspec, true);
+  }
+  // waits for the loads issued before cache_len was read that no product will consume
+  auto drain_spec = [&](int ncache_used, bool q_used) {
+    if (warp != 0 || lane != 0 || a.sort_units) return;
+    bool fine = true;
+    if (!q_used) fine = mbar_wait(&bar_q, 0) && fine;
+    for (int k = ncache_used; k < nspec; ++k) fine = mbar_wait(&bar_kv[k], 0) && fine;
+    if (!fine) set_status(a.status, MARS_DEV_TIMEOUT);
+  };
+
   if (a.sort_units) {
     for (int t = tid; t < a.batch; t += kThreads) s_len[t] = __ldg(a.cache_len + t);
     __syncthreads();
@@ -214,16 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (rank == b_rank) s_b = t;
     }
     __syncthreads();
-  } else {
-    if (tid == 0) s_b = b_rank;
-    __syncthreads();
   }
-  const int b = s_b;
-  const int rem = unit_rank % units_per_b;
-  const int g = rem / a.nhc;
-  const int hc = rem % a.nhc;
-  const int h0 = g * a.G + hc * a.Gc;            // first query head of this unit
-  const int heads = min(a.Gc, a.G - hc * a.Gc);  // real heads in this unit
+  const int b = a.sort_units ? s_b : b_rank;
 
   const int len = a.sort_units ? s_len[b] : __ldg(a.cache_len + b);
   const bool deferred = a.pending != nullptr;
@@ -240,6 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(0, 0, 0, 0);
       }
     }
+    drain_spec(0, false);  // the early loads land before the CTA exits
+    if (warp == 0 && lane == 0 && has_new && !a.sort_units && !mbar_wait(&bar_new, 0))
+      set_status(a.status, MARS_DEV_TIMEOUT);
     __syncthreads();  // tensor memory was allocated before the wait: free it (no product was issued)
     if (warp == 1) {
       tc_fence_after();
@@ -250,67 +319,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // slot validity bitmask: every slot, or (deferred) the pending slots below pend and all placeholders
   const uint32_t vmask = deferred ? ((1u << pend) - 1u) | (((1u << a.B) - 1u) << a.B) : (1u << a.S) - 1u;
   const int nct = (len + kTileKeys - 1) / kTileKeys;  // cache tiles of the unit
-  const int t0 = static_cast<int>((static_cast<long long>(nct) * crank) / a.C);
-  const int t1 = static_cast<int>((static_cast<long long>(nct) * (crank + 1)) / a.C);
-  const int ncache = t1 - t0;
-  const bool has_new = crank == a.C - 1;
-  const int ntiles = ncache + (has_new ? 1 : 0);  // local tile k: cache tile t0 + k, then the new tile
-
-  const uint32_t tile_bytes = C::NB * 128 * a.box_rows;
-  // TMA loads of cache tile k into its ring stage (the stage is free)
-  auto load_tile = [&](int k) {
-    const int st = k % C::NS;
-    const int key0 = (t0 + k) * kTileKeys;
-    const uint32_t kb = ring + st * C::STAGE, vb = kb + C::NB * C::T_BOX;
-    mbar_arrive_expect_tx(&bar_kv[st], 2 * tile_bytes);
-    for (int c = 0; c < C::NB; ++c) {
-      tma_load_4d(kb + c * C::T_BOX, &tm_kc, &bar_kv[st], 64 * c, key0, g, b);
-      tma_load_4d(vb + c * C::T_BOX, &tm_vc, &bar_kv[st], 64 * c, key0, g, b);
-    }
-  };
-  // The loads write rows the zeroing above never touched.  The lanes of warp 0
-  // issue them side by side: lane 0 the Q tile, lane 1 + k the first ring stages'
-  // cache tile k, lane NS + 1 the new-key tile (each has its own barrier).
-  if (warp == 0 && ntiles > 0) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar_q, C::NB * 128 * R * (dup ? 2 : 1));
-      for (int c = 0; c < C::NB; ++c) {
-        tma_load_4d(q_s + c * C::Q_BOX, &tm_q, &bar_q, 64 * c, h0, 0, b);
-        if (dup) tma_load_4d(q_s + c * C::Q_BOX + 32 * 128, &tm_q, &bar_q, 64 * c, h0, 0, b);
-      }
-    } else if (lane <= min(ncache, C::NS)) {
-      load_tile(lane - 1);
-    } else if (lane == C::NS + 1 && has_new) {
-      mbar_arrive_expect_tx(&bar_new, 2 * C::NB * 128 * a.S);
-      for (int c = 0; c < C::NB; ++c) {
-        tma_load_4d(nk_s + c * C::N_BOX, &tm_kn, &bar_new, 64 * c, g, 0, b);
-        tma_load_4d(nv_s + c * C::N_BOX, &tm_vn, &bar_new, 64 * c, g, 0, b);
-      }
-    }
-  }
-
+  const int ncache = nct > crank ? (nct - crank + a.C - 1) / a.C : 0;  // local cache tiles
+  const int ntiles = ncache + (has_new ? 1 : 0);  // local tile k: cache tile crank + k C, then the new tile
+  if (a.sort_units && ntiles > 0) first_loads(b, min(ncache, C::NS), true);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   bool ok = true;
-  // small-unit merge (dup): this thread's half row after combining streams A and B
-  bool push = false;
-  int push_row = 0, push_half = 0;
-  float pc[D / 2];
-  float pc_m = -INFINITY, pc_l = 0.f;
 
   if (warp == 0) {
     // ================= TMA producer: the tiles past the first NS, each into a freed stage
-    // (everything it loads is consumed before the CTA exits)
+    // (everything it loads is consumed, or waited for, before the CTA exits)
     if (lane == 0) {
       for (int k = C::NS; k < ncache; ++k) {
         if (!mbar_wait(&bar_kv_empty[k % C::NS], ((k / C::NS) - 1) & 1)) {
           set_status(a.status, MARS_DEV_TIMEOUT);
           break;
         }
-        load_tile(k);
+        load_tile(k, b);
       }
     }
+    drain_spec(ncache, ntiles > 0);
     __syncwarp();
     if (deferred && has_new && hc == 0) {
       // Commit the valid pending rows of KV head g at the cursor.  Other CTAs of
@@ -401,13 +430,190 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && leader) set_status(a.status, MARS_DEV_TIMEOUT);
     }
     __syncwarp();
+  } else if (split4) {
+    // ================= small unit: the softmax warp of stream x in lane quarter q
+    // (warps 2..5: A, 6..9: B) takes keys [16 q, 16 q + 16) of each of the stream's
+    // tiles for every row (thread = row, the same rows in every quarter).  Its P
+    // goes to columns [8 q, 8 q + 8) of the tile's P and zeros to the other 24, so
+    // the PV product of a quarter's lanes sums its own keys only.
+    const int x = (warp - 2) >> 2;
+    const int q = warp & 3;
+    const int r = lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t s_col = tmem + lane_addr + x * kTileKeys;
+    const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
+    const int slot = r / a.Gc;
+    const bool row_valid = r < R && slot < a.S && ((vmask >> slot) & 1u);
+    const uint32_t new_vis = row_valid ? vmask & ((2u << slot) - 1u) : 0u;
+    float m_used = -INFINITY, l = 0.f;
+    int nmine = 0;
+    for (int k = x; k < ntiles; k += 2, ++nmine) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[x], nmine & 1));
+      if (!ok) break;
+      tc_fence_after();
+      const bool is_new = k >= ncache;
+      const int tile0 = (crank + k * a.C) * kTileKeys;  // first key of the (cache) tile
+      uint32_t sv[16];
+      tmem_ld16(s_col + 16 * q, sv);
+      tc_wait_ld();
+      if (is_new) {
+        // the new-key tile has kNewKeys = 16 keys, all in quarter 0's slice
+#pragma unroll
+        for (int c = 0; c < 16; ++c) sv[c] = (q == 0 && ((new_vis >> c) & 1u)) ? sv[c] : 0xFF800000u;
+      } else {
+        const int vlast = row_valid ? len - 1 - tile0 - 16 * q : -1;  // last visible key of the slice
+        if (vlast < 15) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) sv[c] = c <= vlast ? sv[c] : 0xFF800000u;
+        }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        mx0 = fmaxf(mx0, __uint_as_float(sv[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(sv[c + 1]));
+      }
+      const float tile_max = fmaxf(mx0, mx1) * a.scale_log2;
+      float alpha = 1.f;
+      const bool grow = tile_max > m_used + kRescaleThreshold;
+      if (grow) {
+        alpha = fast_exp2(m_used - tile_max);  // 0 when m_used is -inf
+        m_used = tile_max;
+      }
+      if (nmine > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 16) {
+          uint32_t ov[16];
+          tmem_ld16(o_col + c, ov);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st16(o_col + c, ov);
+        }
+      }
+      const float neg_mu = m_used == -INFINITY ? 0.f : -m_used;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pw[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * e]), a.scale_log2, neg_mu));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), a.scale_log2, neg_mu));
+        sum0 += p0;
+        sum1 += p1;
+        pw[e] = pack_bf16x2(p0, p1);
+      }
+      uint32_t plo[16], phi[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        plo[e] = q == 0 ? pw[e] : 0u;
+        plo[8 + e] = q == 1 ? pw[e] : 0u;
+        phi[e] = q == 2 ? pw[e] : 0u;
+        phi[8 + e] = q == 3 ? pw[e] : 0u;
+      }
+      tmem_st16(s_col, plo);
+      tmem_st16(s_col + 16, phi);
+      l = l * alpha + (sum0 + sum1);
+      // V rows that P = 0 meets must be finite: invalid pending slots of the new tile
+      // (deferred mode) and keys at or past cache_len in the last cache tile
+      if (is_new && deferred && pend < a.B) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_new, 0));
+        if (!ok) break;
+        const int per_box = (a.B - pend) * 8;
+        for (int e = q * 32 + lane; e < C::NB * per_box; e += 128) {
+          const int bx = e / per_box, w = e % per_box;
+          st_shared_v4(nv_s + bx * C::N_BOX + pend * 128 + w * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+      }
+      if (!is_new && len - tile0 < kTileKeys) {
+        const int st = k % C::NS;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_kv[st], (k / C::NS) & 1));
+        if (!ok) break;
+        const int z0 = len - tile0;
+        const int per_box = (kTileKeys - z0) * 8;
+        const uint32_t vb = ring + st * C::STAGE + C::NB * C::T_BOX;
+        for (int e = q * 32 + lane; e < C::NB * per_box; e += 128) {
+          const int bx = e / per_box, w = e % per_box;
+          st_shared_v4(vb + bx * C::T_BOX + z0 * 128 + w * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+      }
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_p[x]);
+    }
+    if (ok && nmine > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[x], 0));
+    if (!ok && lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+    const bool have = ok && nmine > 0;
+    // ---- combine this CTA's 8 states of each row (state w = 4 x + q) through shared
+    // memory; warp w then writes columns [w D / 8, (w + 1) D / 8) of every combined
+    // row, and warp 0 the row's (m, l), into the outbox [32][D + 4]
+    const int wst = x * 4 + q;
+    named_bar_sync(1, 256);  // every product of both streams is complete: the ring is free
+    tc_fence_after();
+    float* xo = reinterpret_cast<float*>(smem + C::RING_OFF);  // [8][32][D], 16-byte units XOR (row & 7)
+    float* xm = xo + 8 * 32 * D;                               // [8][32]
+    float* xl = xm + 8 * 32;                                   // [8][32]
+    float* outbox = xl + 8 * 32;                               // [32][D + 4]
+    {
+      float4* dst = reinterpret_cast<float4*>(xo + (wst * 32 + r) * D);
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(o_col + c, ov);
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                              __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          dst[((c >> 2) + e) ^ (r & 7)] = v;
+        }
+      }
+      xm[wst * 32 + r] = have ? m_used : -INFINITY;
+      xl[wst * 32 + r] = have ? l : 0.f;
+    }
+    named_bar_sync(1, 256);
+    if (r < R) {
+      float ws[8];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        ws[t] = xm[t * 32 + r];
+        mx = fmaxf(mx, ws[t]);
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        ws[t] = ws[t] == -INFINITY ? 0.f : fast_exp2(ws[t] - mx);  // states without keys weigh 0
+        lsum += ws[t] * xl[t * 32 + r];
+      }
+      const float4* x4 = reinterpret_cast<const float4*>(xo);
+      float4* orow = reinterpret_cast<float4*>(outbox + r * (D + 4));
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        const int c4 = wst * (D / 32) + j;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float4 v = x4[(t * 32 + r) * (D / 4) + (c4 ^ (r & 7))];
+          acc.x += ws[t] * v.x;
+          acc.y += ws[t] * v.y;
+          acc.z += ws[t] * v.z;
+          acc.w += ws[t] * v.w;
+        }
+        orow[c4] = acc;
+      }
+      if (wst == 0) orow[D / 4] = make_float4(mx, lsum, 0.f, 0.f);
+    }
+    fence_async_smem();  // the bulk copies (async proxy) read the outbox
+    named_bar_sync(1, 256);
   } else {
     // ================= softmax of stream x (warps 2..5: A, 6..9: B)
     const int x = (warp - 2) >> 2;
     const int quad = warp & 3;  // TMEM lane quarter this warp may access
-    const int qbase = (dup && x == 1) ? 1 : 0;  // first lane quarter holding this stream's rows
-    const int r = (quad - qbase) * 32 + lane;   // query row (rows >= R are padding)
-    const bool active = quad >= qbase && quad - qbase < act_warps;
+    const int r = quad * 32 + lane;
+    const bool active = quad < act_warps;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_col = tmem + lane_addr + x * kTileKeys;
     const uint32_t o_col = tmem + lane_addr + C::O_COL + x * D;
@@ -425,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // last visible column of this tile for this row
         const bool is_new = k >= ncache;
-        const int key0 = (t0 + k) * kTileKeys;
+        const int key0 = (crank + k * a.C) * kTileKeys;
         const int vlast = row_valid ? len - 1 - key0 : -1;
         uint32_t s[kTileKeys];
         tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
@@ -486,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_new, 0));
           if (!ok) break;
           const int per_box = (a.B - pend) * 8;  // 16-byte chunks of rows pend .. B-1
-          for (int e = (quad - qbase) * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
+          for (int e = quad * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
             const int bx = e / per_box, w = e % per_box;
             st_shared_v4(nv_s + bx * C::N_BOX + pend * 128 + w * 16, 0u, 0u, 0u, 0u);
           }
@@ -501,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int z0 = len - key0;
           const int per_box = (kTileKeys - z0) * 8;  // 16-byte chunks
           const uint32_t vb = ring + st * C::STAGE + C::NB * C::T_BOX;
-          for (int e = (quad - qbase) * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
+          for (int e = quad * 32 + lane; e < C::NB * per_box; e += 32 * act_warps) {
             const int bx = e / per_box, w = e % per_box;
             st_shared_v4(vb + bx * C::T_BOX + z0 * 128 + w * 16, 0u, 0u, 0u, 0u);
           }
@@ -563,56 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else if (dup) {
-      // ---- small unit over a cluster: combine streams A and B of each row in this
-      // CTA (through shared memory: their rows sit in different lane quarters), each
-      // thread keeping half of the row's columns for the push after this branch.
-      named_bar_sync(1, 256);  // both streams' products are complete: the ring is free
-      tc_fence_after();
-      float* xo = reinterpret_cast<float*>(smem + C::RING_OFF);  // [2][32][D], 16-byte units XOR (row & 7)
-      float* xm = xo + 2 * 32 * D;                               // [2][32]
-      float* xl = xm + 2 * 32;                                   // [2][32]
-      if (active) {
-        float4* dst = reinterpret_cast<float4*>(xo + (x * 32 + r) * D);
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(o_col + c, ov);
-          tc_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                                __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            dst[((c >> 2) + e) ^ (r & 7)] = v;
-          }
-        }
-        xm[x * 32 + r] = have ? m_used : -INFINITY;
-        xl[x * 32 + r] = have ? l : 0.f;
-      }
-      named_bar_sync(1, 256);
-      if (active && r < R) {
-        const float ma = xm[r], mb = xm[32 + r];
-        const float mx = fmaxf(ma, mb);
-        const float wa = ma == -INFINITY ? 0.f : fast_exp2(ma - mx);
-        const float wb = mb == -INFINITY ? 0.f : fast_exp2(mb - mx);
-        pc_m = mx;
-        pc_l = wa * xl[r] + wb * xl[32 + r];
-        const float4* xa = reinterpret_cast<const float4*>(xo + r * D);         // rows without tiles are zero
-        const float4* xb = reinterpret_cast<const float4*>(xo + (32 + r) * D);
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-          const int c4 = x * (D / 8) + j;
-          const float4 va = xa[c4 ^ (r & 7)], vb = xb[c4 ^ (r & 7)];
-          pc[4 * j] = wa * va.x + wb * vb.x;
-          pc[4 * j + 1] = wa * va.y + wb * vb.y;
-          pc[4 * j + 2] = wa * va.z + wb * vb.z;
-          pc[4 * j + 3] = wa * va.w + wb * vb.w;
-        }
-        push = true;
-        push_row = r;
-        push_half = x;
-      }
     } else {
       // Both streams' products are complete once every softmax warp is past its
       // wait above, so the ring (every loaded tile consumed) can hold the merge state.
@@ -646,69 +802,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   // This CTA finishes rows [r_lo, r_hi): first one weight per (row, state),
   // w = 2^(m - max m) / sum_states(2^(m - max m) l), then O = sum w acc.
   tc_fence_before();
-  if (dup) {
-    // Push: each row's combined state goes into the inbox of the CTA that finishes
-    // the row (rows [crank * rows_per, ...) belong to CTA crank), slot
-    // (row - first owned row) * C + source CTA; 16-byte units XOR (slot & 7).
-    const int rows_per = (R + a.C - 1) / a.C;
-    const uint32_t in_acc = smem_u32(smem + C::INBOX_OFF);
-    const uint32_t in_m = in_acc + C::IN_SLOTS * D * 4, in_l = in_m + C::IN_SLOTS * 4;
-    cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
-    if (push) {
-      const int owner = push_row / rows_per;
-      const int slot = (push_row - owner * rows_per) * a.C + crank;
-      const uint32_t row_l = in_acc + slot * D * 4;  // the slot's address in this CTA's window
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const int c4 = push_half * (D / 8) + j;
-        dsmem_st_f32x4(dsmem_map(row_l + 16 * (c4 ^ (slot & 7)), owner), pc[4 * j], pc[4 * j + 1], pc[4 * j + 2],
-                       pc[4 * j + 3]);
+  if (split4) {
+    // Each owning CTA (rows [o rows_per, (o + 1) rows_per)) receives this CTA's combined
+    // rows as one bulk copy into block `crank` of its inbox, completing on its bar_in.
+    cluster_wait();  // every CTA of the cluster has started and armed its inbox
+    if (warp == 2 && lane == 0) {
+      const uint32_t ob = smem_u32(smem + C::RING_OFF) + 8 * 32 * D * 4 + 2 * 8 * 32 * 4;
+      const uint32_t inbox = smem_u32(smem + C::INBOX_OFF) + crank * rows_per * C::ROWB;
+      for (int o = 0; o < a.C; ++o) {
+        const int n_o = min(rows_per, R - o * rows_per);
+        if (n_o <= 0) continue;
+        bulk_s2s_cluster(dsmem_map(inbox, o), ob + o * rows_per * C::ROWB, n_o * C::ROWB,
+                         dsmem_map(smem_u32(&bar_in), o));
       }
-      if (push_half == 0) {
-        dsmem_st_f32(dsmem_map(in_m + 4 * slot, owner), pc_m);
-        dsmem_st_f32(dsmem_map(in_l + 4 * slot, owner), pc_l);
-      }
+      bulk_commit_group();
     }
-    cluster_arrive_release();
-    cluster_wait();  // every push into this CTA's inbox has landed
-    // Finish the owned rows from local shared memory: one weight per (row, source),
+    // Finish the owned rows from the inbox: one weight per (row, source),
     // w = 2^(m - max m) / sum(2^(m - max m) l), then O = sum w acc.
-    const int r_lo = crank * rows_per, r_hi = min(R, r_lo + rows_per);
-    const int nrow = max(0, r_hi - r_lo);
-    float* w_s = reinterpret_cast<float*>(smem + C::RING_OFF);  // [rows_per][C] (the ring is free)
-    const float* acc_in = reinterpret_cast<const float*>(smem + C::INBOX_OFF);
-    const float* m_in = acc_in + C::IN_SLOTS * D;
-    const float* l_in = m_in + C::IN_SLOTS;
-    for (int t0 = 0; t0 < nrow * a.C; t0 += kThreads) {  // uniform trip count: every lane shuffles
-      const int t = t0 + tid;
-      const bool valid = t < nrow * a.C;
-      const float m = valid ? m_in[t] : -INFINITY, l = valid ? l_in[t] : 0.f;  // slot t = (row, source)
-      float mmax = m;
-      for (int o = a.C >> 1; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
-      const float w = m == -INFINITY ? 0.f : fast_exp2(m - mmax);
-      float lsum = w * l;
-      for (int o = a.C >> 1; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-      if (valid) w_s[t] = lsum > 0.f ? w / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
-    }
-    __syncthreads();
-    for (int e = tid; e < nrow * (D / 4); e += kThreads) {
-      const int rr = e / (D / 4), d4 = e % (D / 4);
-      const int r = r_lo + rr;
-      const int i = r / a.Gc, hl = r % a.Gc;
-      if (hl >= heads) continue;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < a.C; ++c) {
-        const int slot = rr * a.C + c;
-        const float w = w_s[slot];
-        const float4 v = reinterpret_cast<const float4*>(acc_in + slot * D)[d4 ^ (slot & 7)];
-        o.x += w * v.x;
-        o.y += w * v.y;
-        o.z += w * v.z;
-        o.w += w * v.w;
+    const bool got = nrow_own == 0 || __syncthreads_and(mbar_wait(&bar_in, 0));
+    if (!got) {
+      if (tid == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+    } else if (nrow_own > 0) {
+      const float* in = reinterpret_cast<const float*>(smem + C::INBOX_OFF);  // [C][rows_per][D + 4]
+      for (int t0 = 0; t0 < nrow_own * a.C; t0 += kThreads) {  // uniform trip count: every lane shuffles
+        const int t = t0 + tid;  // (row rr, source c) = (t / C, t % C)
+        const bool valid = t < nrow_own * a.C;
+        const float* st = in + ((t % a.C) * rows_per + t / a.C) * (D + 4);
+        const float m = valid ? st[D] : -INFINITY, l = valid ? st[D + 1] : 0.f;
+        float mmax = m;
+        for (int o = a.C >> 1; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+        const float w = m == -INFINITY ? 0.f : fast_exp2(m - mmax);
+        float lsum = w * l;
+        for (int o = a.C >> 1; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        if (valid) s_wmerge[t] = lsum > 0.f ? w / lsum : 0.f;  // 0: a row that sees no key (invalid slot)
       }
-      uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+      __syncthreads();
+      for (int e = tid; e < nrow_own * (D / 4); e += kThreads) {
+        const int rr = e / (D / 4), d4 = e % (D / 4);
+        const int r = crank * rows_per + rr;
+        const int i = r / a.Gc, hl = r % a.Gc;
+        if (hl >= heads) continue;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < a.C; ++c) {
+          const float w = s_wmerge[rr * a.C + c];
+          const float4 v = reinterpret_cast<const float4*>(in + (c * rows_per + rr) * (D + 4))[d4];
+          o.x += w * v.x;
+          o.y += w * v.y;
+          o.z += w * v.z;
+          o.w += w * v.w;
+        }
+        uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+      }
     }
+    if (warp == 2 && lane == 0) bulk_wait_read_all();  // the outbox has been read: this CTA may exit
     __syncthreads();  // every tensor-memory read of the epilogue is done
   } else if (a.C > 1) {
     cluster_sync();
