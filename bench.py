@@ -1,17 +1,18 @@
 """Benchmark of the MARS hot path on GB300 (one JSON line on rank 0).
 
 One step runs every stage of the path on synthetic Qwen2.5-shaped inputs:
-  * one decode step at batch 1 (cache 2048, B=4): decode attention + accept,
-    launched as one CUDA graph per step (its kernels are shorter than a host
-    launch call)
+  * one decode step at batch 1 (cache 2048, B=4): decode attention + accept
   * mars_train_attn on the Qwen2.5-7B-shaped batch (b2, L=2048, B=8, 28/4, D=128)
   * mars_train_attn on the Qwen2.5-0.5B-shaped training batch (b4, L=1024,
     B=4, 14/2 heads, D=64)                          -> headline value, TFLOP/s
   * one sliding-window decode step at batch 64 (varlen caches 256..4096, B=8,
     28/4 heads, D=128, V=152064): mars_decode_attn then mars_accept (+ KV append)
-Every kernel (and the batch-1 graph) is timed with CUDA events on the stream it
-runs on; inputs rotate over enough buffers that each kernel's working set
-exceeds twice the L2, so nothing is served from a warm L2 between iterations.
+Each decode step is launched as one CUDA graph per step, as a decode loop runs;
+the training kernels are plain launches.  CUDA events on the launching stream
+bracket every kernel and graph; inputs rotate over enough buffers that each
+kernel's working set exceeds twice the L2, so nothing is served from a warm L2
+between iterations.  The decode kernels' own rates come from graphs of
+back-to-back launches of one kernel.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this build)
 on bounded samples of the same workload.
@@ -335,19 +336,23 @@ def run_gpu(args, rank, world, local):
     ncommit64 = torch.zeros((total, dec64.s.batch), dtype=torch.int32, device=device)
     ncommit1 = torch.zeros((total, dec1.s.batch), dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream()
-    # One step: the batch-1 decode step (decode attention + accept, launched as one
-    # CUDA graph per step, as a small-batch decode loop runs), then the two training
-    # shapes and the batch-64 decode step.  The order keeps a long kernel in front of
-    # each short one, so the host's launch calls never leave the GPU waiting between
-    # the events around a kernel.
-    names = ["decode_step_b1", "train_7b", "train_05b", "decode_attn_b64", "accept_b64"]
-    kernels = ["train_7b", "train_05b", "decode_attn_b64", "accept_b64"]
+    # One step: the batch-1 decode step, the two training shapes, then the batch-64
+    # decode step.  Each decode step (decode attention + accept) is launched as one
+    # CUDA graph per step, as a decode loop runs; the training kernels are plain
+    # launches.  The host's launch calls stay ahead of the GPU, so no host gap lands
+    # inside the events around a kernel or a graph.
+    names = ["decode_step_b1", "train_7b", "train_05b", "decode_step_b64"]
+    kernels = ["train_7b", "train_05b"]
     records64, records1 = [], []
-    b1_graphs = {}
+    b1_graphs, b64_graphs = {}, {}
 
     def b1_calls(i):
         dec1.run_decode(mars, i)
         dec1.run_accept(mars, i, ncommit1[i])
+
+    def b64_calls(i):
+        dec64.run_decode(mars, i)
+        dec64.run_accept(mars, i, ncommit64[i])
 
     def step(i, ev):
         if i % dec64.episode == 0:
@@ -371,30 +376,31 @@ def run_gpu(args, rank, world, local):
         train05.run(mars, i)
         if ev is not None:
             ev[3].record(stream)
-        dec64.run_decode(mars, i)
-        if ev is not None:
-            ev[4].record(stream)
-        dec64.run_accept(mars, i, ncommit64[i])
+        if i in b64_graphs:
+            b64_graphs[i].replay()
+        else:
+            b64_calls(i)
         records64.append(("step", i % dec64.nsets, i))
         if ev is not None:
-            ev[5].record(stream)
+            ev[4].record(stream)
 
     for i in range(args.warmup):
         step(i, None)
     torch.cuda.synchronize()
-    # the batch-1 decode step of every timed step, captured ahead of the timed region
+    # the decode steps of every timed step, captured ahead of the timed region
     pool = torch.cuda.graph_pool_handle()
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
         for i in range(args.warmup, args.warmup + args.steps):
-            g = torch.cuda.CUDAGraph()
-            g.capture_begin(pool=pool)
-            b1_calls(i)
-            g.capture_end()
-            b1_graphs[i] = g
+            for graphs, calls in ((b1_graphs, b1_calls), (b64_graphs, b64_calls)):
+                g = torch.cuda.CUDAGraph()
+                g.capture_begin(pool=pool)
+                calls(i)
+                g.capture_end()
+                graphs[i] = g
     stream.wait_stream(cap)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier(dist, world)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
@@ -429,8 +435,6 @@ def run_gpu(args, rank, world, local):
     work = {
         "train_05b": ("tensor", [train05.flops] * args.steps, "TFLOP/s", 1e-12),
         "train_7b": ("tensor", [train7.flops] * args.steps, "TFLOP/s", 1e-12),
-        "decode_attn_b64": ("hbm", dec64_b[timed], "GB/s", 1e-9),
-        "accept_b64": ("hbm", acc64_b[timed], "GB/s", 1e-9),
     }
     traffic = ncu_traffic()
     parts = {}
@@ -446,8 +450,7 @@ def run_gpu(args, rank, world, local):
         if bound == "tensor":
             parts[n]["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
     for tag, ms, byts, hist in (
-            ("b64", sum(per_kernel_ms["decode_attn_b64"]) + sum(per_kernel_ms["accept_b64"]),
-             sum(dec64_b[timed]) + sum(acc64_b[timed]), n64),
+            ("b64", sum(per_kernel_ms["decode_step_b64"]), sum(dec64_b[timed]) + sum(acc64_b[timed]), n64),
             ("b1", sum(per_kernel_ms["decode_step_b1"]), sum(dec1_b[timed]) + sum(acc1_b[timed]), n1)):
         parts[f"decode_step_{tag}"] = {
             "steps_per_s": round(args.steps / (ms * 1e-3), 1),
@@ -455,7 +458,8 @@ def run_gpu(args, rank, world, local):
             "frac_of_hbm": round(byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "tokens_per_step": round(float(hist[timed].sum(axis=1).mean()), 3),
         }
-    parts["decode_step_b1"]["in_step"] = "one CUDA graph per step (decode attention + accept)"
+    for tag in ("b1", "b64"):
+        parts[f"decode_step_{tag}"]["in_step"] = "one CUDA graph per step (decode attention + accept)"
     # The training shapes also as planned for them: back-to-back launches between two
     # CUDA events (inputs rotating over the same >= 2x L2 buffer sets), median of 5.
     for n, w in (("train_05b", train05), ("train_7b", train7)):
@@ -473,14 +477,14 @@ def run_gpu(args, rank, world, local):
         ach = w.flops / (us * 1e-6) * 1e-12
         parts[n]["back_to_back"] = {"avg_us": round(us, 3), "launches": 200, "median_of": 5,
                                     "achieved": round(ach, 2), "frac": round(ach / peaks["bf16_tflops"], 4)}
-    # The batch-64 decode kernels also back to back (a CUDA graph of 64 launches over
-    # the rotating buffer sets, each launch's set-up overlapping the previous one's
-    # tail as in a decode loop): the kernels' own device rate.
-    for n, kind in (("decode_attn_b64", "decode"), ("accept_b64", "accept")):
-        us, byts = run_graph_kernel(mars, dec64, kind, n_launches=64)
-        ach = byts / (us * 1e-6) / 1e9
-        parts[n]["back_to_back"] = {"avg_us": round(us, 3), "launches": 64, "timing": "one CUDA graph",
-                                    "achieved": round(ach, 2), "frac": round(ach / peaks["hbm_gbs"], 4)}
+    # The decode kernels' own device rates: a CUDA graph of back-to-back launches of
+    # one kernel over the rotating buffer sets (64 at batch 64, 256 at batch 1), each
+    # launch's set-up overlapping the previous one's tail as in a decode loop.
+    for n, kind, work_, nl in (("decode_attn_b64", "decode", dec64, 64), ("accept_b64", "accept", dec64, 64),
+                               ("decode_attn_b1", "decode", dec1, 256), ("accept_b1", "accept", dec1, 256)):
+        us, byts = run_graph_kernel(mars, work_, kind, n_launches=nl)
+        parts[n] = {"avg_us": round(us, 3), "timing": f"{nl} back-to-back launches in one CUDA graph",
+                    "roofline": roofline("hbm", byts / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s", traffic.get(n))}
     dominant = max(kernels, key=lambda n: sum(per_kernel_ms[n]))
 
     # headline: training-mask attention TFLOP/s on the Qwen2.5-0.5B-shaped batch
@@ -495,14 +499,6 @@ def run_gpu(args, rank, world, local):
         # the batch-1 workload's four thresholds, each a 256-step episode in one graph
         parts["decode_step_b1"]["tau_sweep"] = {
             str(tau): run_graph(mars, dec1, device, peaks["hbm_gbs"], tau=tau) for tau in dec1.s.taus}
-        # Batch-1 kernels are shorter than a host launch, so the in-step event times
-        # above include host gaps: their roofline comes from 256 launches of the one
-        # kernel captured in a graph (rotating buffer sets), device time per launch.
-        for n, kind in (("decode_attn_b1", "decode"), ("accept_b1", "accept")):
-            us, byts = run_graph_kernel(mars, dec1, kind)
-            parts[n] = {"avg_us": round(us, 3), "timing": "256 launches in one CUDA graph",
-                        "roofline": roofline("hbm", byts / (us * 1e-6) / 1e9, peaks["hbm_gbs"], "GB/s",
-                                             traffic.get(n))}
     # variants of the accept row, timed on their own after the step loop: the margin
     # gate and the batch-minimum cache mode (the paper's original sampler)
     parts["accept_margin_b64"] = run_accept_variant(args, mars, dec64, device, peaks["hbm_gbs"], traffic,
@@ -541,7 +537,7 @@ def run_gpu(args, rank, world, local):
         "parts": parts,
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": 8 * args.steps,  # 2 train, 2 decode, 2 x (accept stream + finish); b1 pair in a graph
+        "gpu_launches": 8 * args.steps,  # 2 train, 2 decode, 2 x (accept stream + finish); decode pairs in graphs
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
