@@ -56,6 +56,8 @@ __all__ = [
     "accept",
     "append_kv",
     "accept_deferred",
+    "lm_head_logits",
+    "lm_head_accept",
     "near_threshold",
 ]
 
@@ -337,6 +339,22 @@ def accept(logits, tau: float, gate: str = "prob", batch_min: bool = False):
     if batch_min:
         n = np.full_like(n, n.min())
     return tokens, conf, n
+
+
+def lm_head_logits(hidden, weight):
+    """Logits of the LM head for the proposal positions: logits[..., v] =
+    sum_k hidden[..., k] * weight[v, k] (fp64), with weight in the [V, hidden]
+    layout of the head's linear map.  The MARS blog post ("Where it stands
+    against the alternatives") names this 152k-vocabulary projection as the
+    drafter's cost; the acceptance step reads its output."""
+    return np.asarray(hidden, dtype=np.float64) @ np.asarray(weight, dtype=np.float64).T
+
+
+def lm_head_accept(hidden, weight, tau: float):
+    """The LM head followed by the acceptance step, as one definition: the
+    tokens, confidences and commit counts of accept() (top-1 probability gate)
+    on lm_head_logits(hidden, weight).  hidden: [b, B, K]; weight: [V, K]."""
+    return accept(lm_head_logits(hidden, weight), tau)
 
 
 def append_kv(k_cache, v_cache, cache_len, k_new, v_new, n_commit):

@@ -592,3 +592,47 @@ def check_append(append_kv):
                 else:
                     assert np.array_equal(kc2[b, g, p], kc[b, g, p])
                     assert np.array_equal(vc2[b, g, p], vc[b, g, p])
+
+
+# --------------------------------------------------------------------------
+# LM head fused with acceptance
+# --------------------------------------------------------------------------
+
+def check_lm_head_logits_bruteforce(lm_head_logits):
+    """Every logit is the dot product of a hidden row with a weight row, written as loops."""
+    h = rand((2, 3, 5), 71)
+    w = rand((7, 5), 72)
+    got = lm_head_logits(h, w)
+    assert got.shape == (2, 3, 7)
+    for b in range(2):
+        for i in range(3):
+            for v in range(7):
+                want = 0.0
+                for k in range(5):
+                    want += h[b, i, k] * w[v, k]
+                assert abs(got[b, i, v] - want) < 1e-12
+
+
+def check_lm_head_logits_one_hot(lm_head_logits):
+    """A one-hot hidden row e_j reads column j of the weight: logits[v] = weight[v, j]."""
+    w = rand((9, 9), 73)  # square, so a transposed weight would still have the right shape
+    for j in (0, 4, 8):
+        h = np.zeros((1, 1, 9))
+        h[0, 0, j] = 1.0
+        assert np.array_equal(lm_head_logits(h, w)[0, 0], w[:, j])
+
+
+def check_lm_head_accept_closed_form(lm_head_accept):
+    """Weight row t = a h / |h|^2 and every other row orthogonal to h: the logits are a
+    at t and 0 elsewhere, so the token is t and conf = 1 / (1 + (V - 1) e^-a)."""
+    K, V = 16, 40
+    g = np.random.default_rng(74)
+    for a, t in [(6.0, 3), (0.7, 0), (12.0, 39)]:
+        h = g.standard_normal(K)
+        w = g.standard_normal((V, K))
+        w -= np.outer(w @ h, h) / (h @ h)  # every row orthogonal to h
+        w[t] = a * h / (h @ h)
+        tok, conf, n = lm_head_accept(h[None, None, :], w, 0.0)
+        assert tok[0, 0] == t
+        assert abs(conf[0, 0] - 1.0 / (1.0 + (V - 1) * np.exp(-a))) < 1e-12
+        assert n[0] == 1

@@ -57,6 +57,9 @@ def all_pins(m):
         "bwd_fd": lambda: pins.check_bwd_finite_differences(m.train_attn_bwd, m.train_attn),
         "bwd_gqa": lambda: pins.check_bwd_gqa_is_repeat_kv(m.train_attn_bwd),
         "bwd_closed": lambda: pins.check_bwd_closed_forms(m.train_attn_bwd),
+        "lm_brute": lambda: pins.check_lm_head_logits_bruteforce(m.lm_head_logits),
+        "lm_one_hot": lambda: pins.check_lm_head_logits_one_hot(m.lm_head_logits),
+        "lm_accept": lambda: pins.check_lm_head_accept_closed_form(m.lm_head_accept),
     }
     failed = []
     for name, fn in checks.items():
@@ -139,6 +142,10 @@ MUTATIONS = [
     ("kc[b, :, ln[b] + i, :] = k_new[b, i, :, :]", "kc[b, :, ln[b] + i + 1, :] = k_new[b, i, :, :]"),
     # length not advanced
     ("ln[b] += n", "ln[b] += 0"),
+    # LM head: the weight used untransposed (columns as vocabulary rows)
+    ("np.asarray(weight, dtype=np.float64).T", "np.asarray(weight, dtype=np.float64)"),
+    # LM head: the acceptance reads the hidden states instead of the logits
+    ("return accept(lm_head_logits(hidden, weight), tau)", "return accept(np.asarray(hidden, dtype=np.float64), tau)"),
 ]
 
 

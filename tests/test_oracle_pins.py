@@ -167,3 +167,15 @@ def test_bwd_gqa_is_repeat_kv():
 
 def test_bwd_closed_forms():
     pins.check_bwd_closed_forms(oracle.train_attn_bwd)
+
+
+def test_lm_head_logits_bruteforce():
+    pins.check_lm_head_logits_bruteforce(oracle.lm_head_logits)
+
+
+def test_lm_head_logits_one_hot():
+    pins.check_lm_head_logits_one_hot(oracle.lm_head_logits)
+
+
+def test_lm_head_accept_closed_form():
+    pins.check_lm_head_accept_closed_form(oracle.lm_head_accept)
