@@ -302,6 +302,37 @@ int mars_accept_margin(const uint16_t* logits, int batch, int B, int V, float ta
                        int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mars_lm_head_accept - the LM head of the proposal positions fused with
+ * mars_accept.  The authors' MARS blog post ("Where it stands against the
+ * alternatives") names the 152k-vocabulary projection that every proposal ends
+ * in as the drafter's cost; here its logits
+ *     logits[b, i, v] = sum_k hidden[b, i, k] * weight[v, k]
+ * are accumulated in fp32 in tensor memory and reduced on the spot to each
+ * row's maximum, lowest argmax and sum of exp(logit - max): they are never
+ * written to memory.  Tokens, conf (top-1 probability, computed from the fp32
+ * logits), the commit rule and the block-level KV append are those of
+ * mars_accept.
+ *
+ *   hidden           [batch, B, K] bf16, the final hidden states of the B proposal
+ *                    positions; K a multiple of 64
+ *   weight           [V, K] bf16, the head's linear map (one row per vocabulary entry)
+ *   workspace        device buffer of >= mars_lm_head_accept_workspace_size(batch,
+ *                    B, V) bytes (one partial per row and vocabulary range);
+ *                    contents on entry do not matter; calls that share it must
+ *                    not overlap in time
+ * Other arguments, outputs and error behaviour as mars_accept; hidden and weight
+ * must be 16-byte aligned.  Two kernel launches on `stream` (the fused head,
+ * then one CTA per sequence for the commit rule and the append).
+ */
+size_t mars_lm_head_accept_workspace_size(int batch, int B, int V);
+int mars_lm_head_accept(const uint16_t* hidden, const uint16_t* weight, int batch, int B, int K, int V, float tau,
+                        const uint16_t* k_new, const uint16_t* v_new,
+                        uint16_t* k_cache, uint16_t* v_cache, int32_t* cache_len,
+                        int Hkv, int D, int cap,
+                        int32_t* tokens, float* conf, int32_t* n_commit,
+                        int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mars_accept_noalloc - mars_accept for callers that cannot allocate device
  * memory.  The MARS pages have no counterpart to this call: it exists for
  * callers such as plugins that only receive the input and output buffers of a

@@ -27,7 +27,8 @@ def lib():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "mars_accept", "mars_accept_ex", "mars_accept_margin", "mars_accept_noalloc", "mars_accept_workspace_size",
-        "mars_decode_attn", "mars_decode_attn_deferred", "mars_decode_attn_workspace_size", "mars_last_cuda_error", "mars_selftest_wait_timeout",
+        "mars_decode_attn", "mars_decode_attn_deferred", "mars_decode_attn_workspace_size", "mars_last_cuda_error", "mars_lm_head_accept",
+        "mars_lm_head_accept_workspace_size", "mars_selftest_wait_timeout",
         "mars_train_attn_bwd", "mars_train_attn_bwd_workspace_size", "mars_status_string", "mars_train_attn", "mars_version"])
 
 

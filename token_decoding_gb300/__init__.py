@@ -16,6 +16,8 @@ from ._lib import (  # noqa: F401
     decode_attn,
     decode_attn_deferred,
     lib,
+    lm_head_accept,
+    lm_head_accept_workspace,
     status_string,
     train_attn,
     train_attn_bwd,

@@ -54,6 +54,9 @@ _SIGNATURES = {
     "mars_accept_ex": (_I, [_P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "mars_accept_noalloc": (_I, [_P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "mars_selftest_wait_timeout": (_I, [_I, ctypes.c_uint, _P, _P, _P]),
+    "mars_lm_head_accept_workspace_size": (_SZ, [_I, _I, _I]),
+    "mars_lm_head_accept": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ,
+                                 _P]),
 }
 
 _lib = None
@@ -385,3 +388,42 @@ def selftest_wait_timeout(withhold: bool, spin_limit: int, status, elapsed_ns=No
         _check(elapsed_ns, "elapsed_ns", torch.int64, (1,), status.device)
     _call("mars_selftest_wait_timeout", 1 if withhold else 0, int(spin_limit), _ptr(status), _ptr(elapsed_ns),
           _stream(stream))
+
+
+def lm_head_accept_workspace(batch: int, B: int, V: int, device) -> torch.Tensor:
+    """A workspace for lm_head_accept (one partial per row and vocabulary range)."""
+    n = int(_fn("mars_lm_head_accept_workspace_size")(batch, B, V))
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def lm_head_accept(hidden, weight, tau: float, k_new, v_new, k_cache, v_cache, cache_len, workspace=None,
+                   tokens=None, conf=None, n_commit=None, status=None, stream=None):
+    """The LM head of the proposal positions fused with accept (include/mars.h:
+    mars_lm_head_accept): hidden [b, B, K], weight [V, K] bf16.  Returns (tokens,
+    conf, n_commit); k_cache, v_cache and cache_len are updated in place."""
+    nb, bq, K = hidden.shape
+    V = weight.shape[0]
+    hkv, d = k_new.shape[2], k_new.shape[3]
+    cap = k_cache.shape[2]
+    dev = hidden.device
+    _check(hidden, "hidden", torch.bfloat16, (nb, bq, K))
+    _check(weight, "weight", torch.bfloat16, (V, K), dev)
+    _check(k_new, "k_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(v_new, "v_new", torch.bfloat16, (nb, bq, hkv, d), dev)
+    _check(k_cache, "k_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(v_cache, "v_cache", torch.bfloat16, (nb, hkv, cap, d), dev)
+    _check(cache_len, "cache_len", torch.int32, (nb,), dev)
+    if workspace is None:
+        workspace = lm_head_accept_workspace(nb, bq, V, dev)
+    tokens = torch.empty((nb, bq), dtype=torch.int32, device=dev) if tokens is None else tokens
+    conf = torch.empty((nb, bq), dtype=torch.float32, device=dev) if conf is None else conf
+    n_commit = torch.empty((nb,), dtype=torch.int32, device=dev) if n_commit is None else n_commit
+    _check(tokens, "tokens", torch.int32, (nb, bq), dev)
+    _check(conf, "conf", torch.float32, (nb, bq), dev)
+    _check(n_commit, "n_commit", torch.int32, (nb,), dev)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,), dev)
+    _call("mars_lm_head_accept", _ptr(hidden), _ptr(weight), nb, bq, K, V, float(tau), _ptr(k_new), _ptr(v_new),
+          _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), hkv, d, cap, _ptr(tokens), _ptr(conf), _ptr(n_commit),
+          _ptr(status), _ptr(workspace), workspace.numel(), _stream(stream))
+    return tokens, conf, n_commit

@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "lm_head.cuh"
 
 namespace {
 
@@ -477,6 +478,8 @@ int configure_kernel() {
   return MARS_OK;
 }
 
+int launch_finish(AcceptArgs& a, cudaStream_t stream);
+
 int launch(AcceptArgs& a, cudaStream_t stream) {
   const int rc = configure_kernel();
   if (rc != MARS_OK) return rc;
@@ -498,8 +501,13 @@ int launch(AcceptArgs& a, cudaStream_t stream) {
                                    : cudaLaunchKernelEx(&cfg, accept_kernel<false>, a);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
   }
-  // The finish launch overlaps its start-up and prefetch with the streaming launch
-  // (programmatic dependent launch); it waits for the partials in-kernel.
+  return launch_finish(a, stream);
+}
+
+// The finish launch (and, in batch-minimum mode, the minimum launch): one CTA per
+// sequence.  It overlaps its start-up and prefetch with the launch that produces
+// the partials (programmatic dependent launch) and waits for them in-kernel.
+int launch_finish(AcceptArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.batch, 1, 1);
   cfg.blockDim = dim3(32 * a.B, 1, 1);
@@ -727,4 +735,44 @@ extern "C" int mars_accept_noalloc(const uint16_t* logits, int batch, int B, int
                            conf, n_commit, status);
   a.partials = reinterpret_cast<Partial*>(scratch);
   return launch(a, static_cast<cudaStream_t>(stream));
+}
+
+// ============================================================================
+// mars_lm_head_accept: the LM head fused with the acceptance step.  The head's
+// kernel (lm_head.cu) reduces each row's logits tile by tile to one partial per
+// vocabulary range; the finish launch above merges them, applies the commit
+// rule and appends, exactly as for mars_accept.
+// ============================================================================
+extern "C" size_t mars_lm_head_accept_workspace_size(int batch, int B, int V) {
+  if (batch <= 0 || B <= 0 || V <= 0) return 0;
+  const int rows = batch * B;
+  return align_up(static_cast<size_t>(rows) * mars_lm_head::splits_for(rows, V) * sizeof(Partial), 256);
+}
+
+extern "C" int mars_lm_head_accept(const uint16_t* hidden, const uint16_t* weight, int batch, int B, int K, int V,
+                                   float tau, const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
+                                   uint16_t* v_cache, int32_t* cache_len, int Hkv, int D, int cap, int32_t* tokens,
+                                   float* conf, int32_t* n_commit, int32_t* status, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  int rc = check_args(hidden, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens, conf,
+                      n_commit, status);
+  if (rc != MARS_OK) return rc;
+  MARS_HOST_CHECK(K >= 64 && K % 64 == 0 && V < (1 << 30), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(mars_host::aligned16(hidden) && weight != nullptr && mars_host::aligned16(weight),
+                  MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(workspace != nullptr && mars_host::aligned16(workspace), MARS_ERR_INVALID_ARG);
+  MARS_HOST_CHECK(workspace_bytes >= mars_lm_head_accept_workspace_size(batch, B, V), MARS_ERR_WORKSPACE_TOO_SMALL);
+  rc = mars_host::check_device();
+  if (rc != MARS_OK) return rc;
+  const int rows = batch * B;
+  const int nsplit = mars_lm_head::splits_for(rows, V);
+  rc = mars_lm_head::launch_partials(hidden, weight, rows, K, V, static_cast<float4*>(workspace), nsplit, status,
+                                     static_cast<cudaStream_t>(stream));
+  if (rc != MARS_OK) return rc;
+  AcceptArgs a = make_args(hidden, batch, B, V, tau, k_new, v_new, k_cache, v_cache, cache_len, Hkv, D, cap, tokens,
+                           conf, n_commit, status);
+  a.partials = static_cast<Partial*>(workspace);
+  a.chunks = nsplit;
+  a.items = rows * nsplit;
+  return launch_finish(a, static_cast<cudaStream_t>(stream));
 }
