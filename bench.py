@@ -511,6 +511,8 @@ def run_gpu(args, rank, world, local):
     # the backward of the training-mask attention on both training shapes
     parts["train_bwd_05b"] = run_train_bwd(args, mars, train05, peaks["bf16_tflops"], traffic, "train_bwd_05b")
     parts["train_bwd_7b"] = run_train_bwd(args, mars, train7, peaks["bf16_tflops"], traffic, "train_bwd_7b")
+    # the LM head of the proposals fused with the acceptance (Qwen2.5-7B head)
+    parts.update(run_lm_head(args, mars, device, peaks, traffic, gen))
 
     # the clock record spans every timed phase above (step loop, back-to-back
     # training launches, e2e, graph episodes, variants, backward)
@@ -755,6 +757,64 @@ def run_train_bwd(args, mars, work, peak, traffic, name):
             "roofline": roofline("tensor", achieved, peak, "TFLOP/s", traffic.get(name))}
 
 
+def run_lm_head(args, mars, device, peaks, traffic, gen):
+    """mars_lm_head_accept with the Qwen2.5-7B head (hidden 3584, V 152064; synthetic
+    weight ~ N(0, 4 / hidden)) for the batch-64 (512 proposal rows) and batch-1 (4
+    rows) decode shapes: min(steps, 20) calls after warm-up, CUDA events on the
+    stream.  Batch 64 is bound by the tensor cores (2 M K V useful FLOPs per call),
+    batch 1 by reading the weight from HBM (2 V K bytes per call)."""
+    import torch
+
+    from token_decoding_gb300 import synth
+
+    K, V = 3584, synth.DECODE_7B_B64.V
+    w = (torch.randn((V, K), generator=gen, device=device) * (2.0 / K ** 0.5)).to(torch.bfloat16)
+    n = max(1, min(args.steps, 20))
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, shape in (("lm_head_accept_b64", synth.DECODE_7B_B64), ("lm_head_accept_b1", synth.DECODE_7B_B1)):
+        s = shape
+        cap = 64 + (n + args.warmup) * s.B
+        h = torch.randn((s.batch, s.B, K), generator=gen, device=device).to(torch.bfloat16)
+        kn = torch.randn((s.batch, s.B, s.Hkv, s.D), generator=gen, device=device).to(torch.bfloat16)
+        kc = torch.zeros((s.batch, s.Hkv, cap, s.D), dtype=torch.bfloat16, device=device)
+        vc = torch.zeros_like(kc)
+        lens = torch.zeros((s.batch,), dtype=torch.int32, device=device)
+        ws = mars.lm_head_accept_workspace(s.batch, s.B, V, device)
+        tok = torch.empty((s.batch, s.B), dtype=torch.int32, device=device)
+        conf = torch.empty((s.batch, s.B), dtype=torch.float32, device=device)
+        nc = torch.empty((s.batch,), dtype=torch.int32, device=device)
+
+        def call():
+            mars.lm_head_accept(h, w, DECODE_TAU, kn, kn, kc, vc, lens, workspace=ws, tokens=tok, conf=conf,
+                                n_commit=nc)
+
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / n
+        rows = s.batch * s.B
+        flops = 2 * rows * K * V
+        if s.batch > 1:
+            ach = flops / (us * 1e-6) / 1e12
+            rl = roofline("tensor", ach, peaks["bf16_tflops"], "TFLOP/s", traffic.get(name))
+        else:
+            ach = 2 * V * K / (us * 1e-6) / 1e9
+            rl = roofline("hbm", ach, peaks["hbm_gbs"], "GB/s", traffic.get(name))
+        out[name] = {"avg_us": round(us, 3), "calls": n, "rows": rows, "hidden": K, "V": V,
+                     "tflop_per_call": round(flops / 1e12, 4), "roofline": rl}
+        del h, kn, kc, vc, ws
+    del w
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_graph(mars, work, device, hbm_peak, tau=DECODE_TAU):
     """A whole decode episode (decode attention + accept per step: 256 steps at batch 1,
     128 at batch 64) captured as one CUDA graph; device-side steps/s, tokens per
@@ -987,7 +1047,19 @@ def run_profile(args):
     gen = torch.Generator(device=device)
     gen.manual_seed(1234)
     part = args.profile
-    if part.startswith("train_bwd"):
+    if part.startswith("lm_head"):
+        K, V = 3584, synth.DECODE_7B_B64.V
+        shape = synth.DECODE_7B_B64 if part.endswith("b64") else synth.DECODE_7B_B1
+        w = (torch.randn((V, K), generator=gen, device=device) * (2.0 / K ** 0.5)).to(torch.bfloat16)
+        h = torch.randn((shape.batch, shape.B, K), generator=gen, device=device).to(torch.bfloat16)
+        kn = torch.randn((shape.batch, shape.B, shape.Hkv, shape.D), generator=gen, device=device).to(torch.bfloat16)
+        kc = torch.zeros((shape.batch, shape.Hkv, 64, shape.D), dtype=torch.bfloat16, device=device)
+        lens = torch.zeros((shape.batch,), dtype=torch.int32, device=device)
+
+        def run(i):
+            lens.zero_()
+            mars.lm_head_accept(h, w, DECODE_TAU, kn, kn, kc, kc, lens)
+    elif part.startswith("train_bwd"):
         w = TrainWork(synth.TRAIN_05B if part == "train_bwd_05b" else synth.TRAIN_7B, device, gen, 0)
         s = w.s
         q, k, v, _ = w.sets[0]
@@ -1048,7 +1120,8 @@ def main():
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph decode episodes (batch 1 and 64)")
     p.add_argument("--profile", choices=["train_05b", "train_7b", "decode_attn_b64", "accept_b64", "decode_attn_b1",
                                          "accept_b1", "accept_margin_b64", "decode_attn_deferred_b64",
-                                         "accept_deferred_b64", "train_bwd_05b", "train_bwd_7b"],
+                                         "accept_deferred_b64", "train_bwd_05b", "train_bwd_7b",
+                                         "lm_head_accept_b64", "lm_head_accept_b1"],
                    help="only launch this kernel, warm-up + steps times, and print no JSON (for ncu)")
     args = p.parse_args()
     if args.steps is None:
