@@ -80,6 +80,19 @@ def test_many_sequences_unsorted_order():
     case(300, 4, 4, 1, 64, 112, lens, 700, sample=[0, 1, 150, 299])
 
 
+@pytest.mark.parametrize("batch,B,hq,hkv,D,lens", [
+    (3, 4, 28, 4, 128, [0, 700, 2040]),   # 28 rows: owners 14 and 15 hold no rows
+    (2, 4, 14, 2, 64, [1, 1999]),          # D = 64, one sequence with a single cache key
+    (1, 1, 17, 1, 64, [1100]),             # 17 rows (odd), one position
+    (2, 2, 16, 1, 128, [64, 1024]),        # 32 rows, cache lengths on tile boundaries
+])
+def test_wide_cluster_small_units(batch, B, hq, hkv, D, lens):
+    """Small units (<= 32 rows) with few units and a long max_len run as 16-CTA
+    clusters where the device schedules them: ranks past a short sequence's tiles hold
+    no keys and ranks past the rows own none."""
+    case(batch, B, hq, hkv, D, 2048 + 64, lens, 750 + hq + D, max_len=2048)
+
+
 def test_max_len_equals_cap():
     case(1, 4, 7, 1, 128, 1000, [1000], 800, max_len=1000)
 

@@ -55,7 +55,8 @@ using namespace mars;
 constexpr int kTileKeys = 64;    // keys per cache tile
 constexpr int kNewKeys = 16;     // N of the new-key tile (B <= 16)
 constexpr int kRows = 128;       // MMA M: query rows of a unit, zero-padded
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 8;   // portable cluster size; the pull merge's state arrays are sized by it
+constexpr int kWideCluster = 16; // small units (<= 32 rows) only, where the device schedules it
 constexpr int kSortLimit = 256;  // sequences; above this units are visited in index order
 constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
@@ -128,7 +129,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-template <int D>
+// kSmall: the small-unit path (<= 32 rows over a cluster) is its own instantiation, so
+// each launch runs only the code it needs (a single wave of CTAs, each running once,
+// fetches its instructions cold).
+template <int D, bool kSmall>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                   const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kn,
@@ -156,7 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // among warps on the four SM sub-partitions (16 keys of each 64-key tile per
   // warp).  A CTA combines its 8 states of a row (2 streams x 4 quarters) and sends
   // each owning CTA its rows with one bulk copy into that CTA's inbox.
-  const bool split4 = R <= 32 && a.C > 1;
+  // The small-unit instantiation compiles only its own path.  The other keeps the
+  // test at run time: compiled without the small path, its register allocation ran
+  // the batch-64 launch 4% slower (55.2 -> 57.4 us, measured), so it keeps both.
+  const bool split4 = kSmall || (R <= 32 && a.C > 1);
   const int rows_per = (R + a.C - 1) / a.C;  // rows finished by each CTA of a small unit
   const int nrow_own = max(0, min(R, (crank + 1) * rows_per) - crank * rows_per);
   if (tid == 0) {
@@ -964,15 +971,33 @@ struct Maps {
   CUtensorMap q, kc, vc, kn, vn;
 };
 
-template <int D>
-int launch(const Maps& mp, const DecodeArgs& a, int units, cudaStream_t stream) {
-  auto kern = decode_kernel<D>;
+template <int D, bool kSmall>
+int launch(const Maps& mp, DecodeArgs a, int units, cudaStream_t stream) {
+  auto kern = decode_kernel<D, kSmall>;
   static bool configured = false;  // per instantiation; the attribute is process-wide
+  static bool wide_ok = false;     // 16-CTA clusters (a non-portable size) can be scheduled
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(kWideCluster, 1, 1);
+      q.blockDim = dim3(kThreads, 1, 1);
+      q.dynamicSmemBytes = DCfg<D>::SMEM;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = kWideCluster;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int n = 0;
+      wide_ok = cudaOccupancyMaxActiveClusters(&n, kern, &q) == cudaSuccess && n >= 4;
+    }
+    cudaGetLastError();  // a refused query leaves no sticky error behind
     configured = true;
   }
+  if (a.C == kWideCluster && !wide_ok) a.C = kMaxCluster;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units * a.C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1049,6 +1074,12 @@ int decode_impl(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
   int cl = pow2_ceil(std::max(1, ceil_div(sms, units)));
   cl = std::min(cl, kMaxCluster);
   while (cl > 1 && cl > max_tiles) cl >>= 1;
+  // Small units (<= 32 rows, the four-quarter path) with few units in the grid take
+  // 16 CTAs each when the tiles allow: half the tiles per CTA for the same merge
+  // (batch 1 of the 7B shape: 10.3 -> 10.1 us at cache 2048, 11.5 -> 10.9 at 3068).
+  // The launch falls back to 8 where the device cannot schedule 16-CTA clusters.
+  if (cl == kMaxCluster && a.Gc * S <= 32 && max_tiles >= kWideCluster && units * kWideCluster <= 2 * sms)
+    cl = kWideCluster;
   a.C = cl;
   a.sort_units = (batch > 1 && batch <= kSortLimit) ? 1 : 0;
   a.box_rows = std::min(cap, kTileKeys);
@@ -1059,8 +1090,12 @@ int decode_impl(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
       !make_map(&mp.vc, v_cache, dc, a.box_rows, 1) || !make_map(&mp.kn, k_new, dn, 1, S) ||
       !make_map(&mp.vn, v_new, dn, 1, S))
     return MARS_ERR_CUDA;
-  return D == 64 ? launch<64>(mp, a, static_cast<int>(units), stream)
-                 : launch<128>(mp, a, static_cast<int>(units), stream);
+  const bool small = a.Gc * S <= 32 && a.C > 1;
+  if (D == 64)
+    return small ? launch<64, true>(mp, a, static_cast<int>(units), stream)
+                 : launch<64, false>(mp, a, static_cast<int>(units), stream);
+  return small ? launch<128, true>(mp, a, static_cast<int>(units), stream)
+               : launch<128, false>(mp, a, static_cast<int>(units), stream);
 }
 
 }  // namespace
