@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_fixed, bar_ffree, bar_stage[C::NSLOT], bar_free[C::NSLOT], bar_s, bar_sdp, bar_p, bar_pfree,
-      bar_acc;
+      bar_acc, bar_stg;
   __shared__ uint32_t tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -239,20 +239,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = 2 * a.nt;
   const int per_tile = a.batch * a.Hq;
   const int nunits = ntiles * per_tile;
+  // A unit's steps: every query tile that sees its key tile (dKV), or every key tile
+  // its query tile sees (dQ), in index order.  The conditions of Eq. 2 are monotonic
+  // in the other tile's index within a stream, so those tiles form one range per
+  // stream, [lo0, hi0) among the clean tiles and [lo1, hi1) among the noisy ones.
+  // The producer finds the ranges once per unit and publishes them with the unit.
   struct Unit {
-    int tile, b, hh, g, u0, uend, nsteps;
+    int tile, b, hh, g, u0, uend, nsteps, lo0, hi0, lo1, hi1;
   };
   __shared__ int unit_q[4];
+  __shared__ int4 unit_rng[4];
   __shared__ __align__(8) uint64_t bar_unit[4];
-  auto unit_of = [&](int u, Unit& U) {
+  auto unit_base = [&](int u, Unit& U) {
     U.tile = order.tile[u / per_tile];
     const int rest = static_cast<int>(u % per_tile);
     U.b = rest / a.Hq;
     U.hh = rest % a.Hq;  // the query head
     U.g = U.hh / a.G;    // its KV head
     tile_rows(a, U.tile, U.u0, U.uend);
-    U.nsteps = 0;
-    for (int o = 0; o < ntiles; ++o) U.nsteps += MODE == kDKV ? tile_visible(a, o, U.tile) : tile_visible(a, U.tile, o);
+  };
+  auto set_ranges = [&](Unit& U, int lo0, int hi0, int lo1, int hi1) {
+    U.lo0 = lo0, U.hi0 = hi0, U.lo1 = lo1, U.hi1 = hi1;
+    U.nsteps = (hi0 - lo0) + (hi1 - lo1);
+  };
+  auto scan_ranges = [&](Unit& U) {  // producer: the visible tiles of each stream
+    int lo[2] = {-1, -1}, hi[2] = {0, 0};
+    for (int o = 0; o < ntiles; ++o) {
+      if (MODE == kDKV ? tile_visible(a, o, U.tile) : tile_visible(a, U.tile, o)) {
+        const int st = o >= a.nt;
+        if (lo[st] < 0) lo[st] = o;
+        hi[st] = o + 1;
+      }
+    }
+    if (lo[0] < 0) lo[0] = hi[0] = 0;               // empty clean range
+    if (lo[1] < 0) lo[1] = hi[1] = ntiles;          // empty noisy range
+    set_ranges(U, lo[0], hi[0], lo[1], hi[1]);
   };
   // the r-th unit of this CTA as the consumers see it: false at the end (or on a timeout)
   auto unit = [&](int r, Unit& U) -> bool {
@@ -262,14 +283,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int u = unit_q[r & 3];
     if (u < 0) return false;
-    unit_of(u, U);
+    unit_base(u, U);
+    const int4 rg = unit_rng[r & 3];
+    set_ranges(U, rg.x, rg.y, rg.z, rg.w);
     return true;
   };
-  // The steps of a unit: every query tile that sees its key tile (dKV), or every key
-  // tile its query tile sees (dQ), in index order; each role walks them itself.
-  auto next_other = [&](const Unit& U, int o) {  // the first such tile after o
-    while (++o < ntiles && !(MODE == kDKV ? tile_visible(a, o, U.tile) : tile_visible(a, U.tile, o))) {
-    }
+  // the unit's first step tile after o (o = -1: its first)
+  auto next_other = [&](const Unit& U, int o) {
+    ++o;
+    if (o < U.lo0) o = U.lo0;
+    if (o >= U.hi0 && o < U.lo1) o = U.lo1;
     return o;
   };
 
@@ -285,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_p, 128 * kEW);
     mbar_init(&bar_pfree, 1);  // step n's accumulating products are complete
     mbar_init(&bar_acc, 1);
+    mbar_init(&bar_stg, 128 * kEW);  // every elementwise warp has written its staged epilogue block out
     for (int s = 0; s < 4; ++s) mbar_init(&bar_unit[s], 1);
     fence_mbar_init();
   }
@@ -326,10 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       Unit U;
       for (int r = 0; ok; ++r) {
         const int u = r == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(a.next_unit, 1);
+        if (u < nunits) {
+          unit_base(u, U);
+          scan_ranges(U);
+          unit_rng[r & 3] = make_int4(U.lo0, U.hi0, U.lo1, U.hi1);
+        }
         unit_q[r & 3] = u < nunits ? u : -1;
         mbar_arrive(&bar_unit[r & 3]);  // release: the slot is written
         if (u >= nunits) break;
-        unit_of(u, U);
         // fixed operands: K, V of the key tile (dKV) or Q, dO of the query tile (dQ),
         // once the previous unit's last S and dP have read theirs
         if (r > 0 && !mbar_wait(&bar_ffree, (r - 1) & 1)) {
@@ -512,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     int gs = 0, nacc = 0;  // steps done (over all units), units whose accumulators were read
+    int nstg = 0;          // epilogue blocks written out (phases of bar_stg)
     Unit U;
     for (int ur = 0; ok && unit(ur, U); ++ur) {
       const int b = U.b, hh = U.hh, g = U.g, tile = U.tile, u0 = U.u0, uend = U.uend, nsteps = U.nsteps;
@@ -627,55 +656,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         nacc += nsteps > 0;
         tc_fence_after();
-        const int row = u0 + r;
-        const bool store = row < uend;
-        const size_t srow = static_cast<size_t>(b) * (2 * a.L) + (store ? row : 0);
         // The accumulator columns are split evenly over the warpgroups: dK then dV
-        // (dKV mode) or dQ (dQ mode), 16 columns at a time.
+        // (dKV mode) or dQ (dQ mode).  Warp (ew, quad) owns rows [32 quad, 32 quad + 32)
+        // of the unit's tile and columns [c_lo, c_lo + SPAN) of accumulator m.
         constexpr int NACC = MODE == kDKV ? 2 : 1;
         constexpr int SPAN = NACC * D / kEW;  // columns per warpgroup, a multiple of 16
-        static_assert(SPAN % 16 == 0 && D % SPAN == 0, "accumulator split");
+        static_assert(SPAN % 16 == 0 && D % SPAN == 0 && SPAN % 64 == 0 || MODE == kDQ, "accumulator split");
         const int m = (SPAN * ew) / D;
-        const int c_lo = (SPAN * ew) % D, c_hi = c_lo + SPAN;
-        {
-          const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
-          if (MODE == kDKV && a.part != nullptr) {
-            // fp32 partial of this query head, summed over the group by reduce_kernel
-            float4* out = reinterpret_cast<float4*>(a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + srow) *
-                                                                  a.Hq + hh) * D);
+        const int c_lo = (SPAN * ew) % D;
+        const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
+        const bool fp32_out = MODE == kDKV && a.part != nullptr;  // GQA: the query head's fp32 partial
+        // The block leaves through shared memory, so that every global store writes
+        // whole rows of consecutive addresses (a lane per row would scatter each store
+        // instruction over 32 rows): the lane stages its row, 16-byte chunks XOR-swizzled
+        // by the row, then the warp stores row after row.  The P / dS tiles are free
+        // here (every product of the unit is complete): 8 KB per warp in dKV mode (P and
+        // dS, 64 KB), 4 KB in dQ mode (dS, 32 KB).
+        constexpr int STG = MODE == kDKV ? 8192 : 4096;
+        static_assert(8 * STG <= (MODE == kDKV ? 4 : 2) * kBox && 2 * SPAN * 32 <= STG, "staging");
+        const uint32_t stg = (MODE == kDKV ? p_s : ds_s) + static_cast<uint32_t>(warp - 2) * STG;
+        // a staged block: 64 fp32 columns (256-byte rows) or all SPAN bf16 columns
+        const int nblk = fp32_out ? SPAN / 64 : 1;
+        const int cw = fp32_out ? 64 : SPAN;        // columns of a block
+        const int rb = fp32_out ? 256 : 2 * SPAN;   // bytes of a staged row (<= 256)
+        const int cpr = rb / 16;                    // 16-byte chunks per row: 4, 8 or 16
+        const size_t plane = static_cast<size_t>(b) * (2 * a.L);
+        for (int blk = 0; blk < nblk; ++blk) {
+          const int c0 = c_lo + blk * cw;
+          // W columns per batch of tensor-memory loads, awaited once
+          constexpr int W = MODE == kDKV ? 64 : SPAN;
 #pragma unroll 1
-            for (int c = c_lo; c < c_hi; c += 16) {
-              uint32_t v[16];
-              tmem_ld16(tmem + lane_addr + C::ACC_COL + m * D + c, v);
-              tc_wait_ld();
-              if (store) {
+          for (int c = 0; c < cw; c += W) {
+            uint32_t v[W];
 #pragma unroll
-                for (int w = 0; w < 4; ++w)
-                  out[(c >> 2) + w] = nsteps > 0 ? make_float4(__uint_as_float(v[4 * w]) * f, __uint_as_float(v[4 * w + 1]) * f,
-                                                               __uint_as_float(v[4 * w + 2]) * f, __uint_as_float(v[4 * w + 3]) * f)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int x = 0; x < W; x += 32)
+              tmem_ld32(tmem + lane_addr + C::ACC_COL + m * D + c0 + c + x, *reinterpret_cast<uint32_t(*)[32]>(&v[x]));
+            tc_wait_ld();
+            if (fp32_out) {
+#pragma unroll
+              for (int w = 0; w < W / 4; ++w) {
+                const int ch = c / 4 + w;
+                const uint32_t x0 = nsteps > 0 ? __float_as_uint(__uint_as_float(v[4 * w]) * f) : 0u;
+                const uint32_t x1 = nsteps > 0 ? __float_as_uint(__uint_as_float(v[4 * w + 1]) * f) : 0u;
+                const uint32_t x2 = nsteps > 0 ? __float_as_uint(__uint_as_float(v[4 * w + 2]) * f) : 0u;
+                const uint32_t x3 = nsteps > 0 ? __float_as_uint(__uint_as_float(v[4 * w + 3]) * f) : 0u;
+                st_shared_v4(stg + lane * rb + ((ch ^ (lane & (cpr - 1))) << 4), x0, x1, x2, x3);
               }
-            }
-          } else {
-            uint16_t* dst = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
-            const int H = MODE == kDKV ? a.Hkv : a.Hq;
-            const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
-            uint4* out = reinterpret_cast<uint4*>(dst + (srow * H + hout) * D);
-#pragma unroll 1
-            for (int c = c_lo; c < c_hi; c += 16) {
-              uint32_t v[16];
-              tmem_ld16(tmem + lane_addr + C::ACC_COL + m * D + c, v);
-              tc_wait_ld();
-              uint32_t pk[8];
+            } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * f, __uint_as_float(v[2 * e + 1]) * f) : 0u;
-              if (store) {
+              for (int w = 0; w < W / 8; ++w) {
+                uint32_t pk[4];
 #pragma unroll
-                for (int w = 0; w < 2; ++w) out[(c >> 3) + w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                for (int e = 0; e < 4; ++e)
+                  pk[e] = nsteps > 0 ? pack_bf16x2(__uint_as_float(v[8 * w + 2 * e]) * f, __uint_as_float(v[8 * w + 2 * e + 1]) * f)
+                                     : 0u;
+                const int ch = c / 8 + w;
+                st_shared_v4(stg + lane * rb + ((ch ^ (lane & (cpr - 1))) << 4), pk[0], pk[1], pk[2], pk[3]);
               }
             }
           }
+          __syncwarp();
+          // lane l stores chunk l % cpr of row j: 32 / cpr rows per instruction
+          const int rpi = 32 / cpr;
+#pragma unroll 1
+          for (int j0 = 0; j0 < 32; j0 += rpi) {
+            const int j = j0 + lane / cpr, ch = lane % cpr;
+            const uint4 w4 = ld_shared_v4(stg + j * rb + ((ch ^ (j & (cpr - 1))) << 4));
+            const int grow = u0 + quad * 32 + j;
+            if (grow < uend) {
+              if (fp32_out) {
+                float* dst = a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + plane + grow) * a.Hq + hh) * D + c0;
+                reinterpret_cast<uint4*>(dst)[ch] = w4;
+              } else {
+                uint16_t* base = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
+                const int H = MODE == kDKV ? a.Hkv : a.Hq;
+                const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
+                reinterpret_cast<uint4*>(base + ((plane + grow) * H + hout) * D + c0)[ch] = w4;
+              }
+            }
+          }
+          __syncwarp();
+        }
+        // Every elementwise warp has read its staged block before any of them writes
+        // the next unit's P / dS into these tiles (a bounded wait, like every other).
+        mbar_arrive(&bar_stg);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_stg, nstg & 1));
+        ++nstg;
+        if (!ok) {
+          if (lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
+          break;
         }
       }
     }
