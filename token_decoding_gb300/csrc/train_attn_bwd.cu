@@ -90,8 +90,20 @@ struct BCfg {
   static_assert(ACC_COL + (MODE == kDKV ? 2 : 1) * D <= 512, "tensor memory");
 };
 
+// Work units, heaviest first.  An entry is (tile, chunk, chunks): bits 0..15 the
+// tile (0 .. 2 nt - 1), 16..23 the chunk, 24..31 the number of chunks its GQA group
+// is split into.  dKV: entry x (batch, KV head) units, each summing dK, dV over the
+// chunk's query heads (one chunk: the whole group, written as bf16 directly; more:
+// an fp32 partial per chunk, summed by reduce_kernel).  dQ: entry x (batch, query
+// head) units, one chunk each.
+constexpr int kMaxEntries = 4096;
 struct UnitOrder {
-  uint16_t tile[kMaxTiles];  // tile indices (0 .. 2 * nt - 1), heaviest first
+  uint32_t entry[kMaxEntries];
+  int n;
+};
+// Chunks per tile (dKV), for reduce_kernel: tiles with one chunk are already final.
+struct ChunkTable {
+  uint8_t nch[kMaxTiles];
 };
 
 struct BwdArgs {
@@ -183,13 +195,16 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint16_t* __restrict__
 }
 
 // ---------------------------------------------------------------- GQA reduction
-// dK (m = 0) and dV (m = 1) of KV head g: the sum over its G query heads' fp32
-// partials, in head order, rounded once to bf16.  Thread = 8 consecutive elements.
+// dK (m = 0) and dV (m = 1) of KV head g on the key tiles whose GQA group was split
+// into chunks: the sum of the chunks' fp32 partials (slots g G + c), in chunk order,
+// rounded once to bf16.  Tiles of one chunk were written by the dK/dV pass.  Thread =
+// 8 consecutive elements.
 __global__ void __launch_bounds__(256) reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ dk,
-                                                     uint16_t* __restrict__ dv, int batch, int n2, int Hkv, int G,
-                                                     int D) {
+                                                     uint16_t* __restrict__ dv, int batch, int L, int nt, int Hkv,
+                                                     int G, int D, const __grid_constant__ ChunkTable ct) {
   griddep_wait();  // programmatic dependent launch, as delta_kernel
   griddep_launch_dependents();
+  const int n2 = 2 * L;
   const long long e8 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long per_m = static_cast<long long>(batch) * n2 * Hkv * D / 8;
   if (e8 >= 2 * per_m) return;
@@ -199,10 +214,13 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float* __restrict__ p
   const long long rg = r / (D / 8);  // (b, i, g)
   const int g = static_cast<int>(rg % Hkv);
   const long long bi = rg / Hkv;
+  const int i = static_cast<int>(bi % n2);
+  const int nch = ct.nch[i < L ? i / kT : nt + (i - L) / kT];
+  if (nch <= 1) return;  // final already
   const int Hq = Hkv * G;
   const float* src = part + ((static_cast<size_t>(m) * batch * n2 + bi) * Hq + static_cast<size_t>(g) * G) * D + 8 * dc;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < nch; ++h) {
     const float4 x = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(h) * D));
     const float4 y = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(h) * D + 4));
     acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
@@ -237,30 +255,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   // S, which comes after the elementwise warps' P of unit r - 1), so four slots
   // suffice.
   const int ntiles = 2 * a.nt;
-  const int per_tile = a.batch * a.Hq;
-  const int nunits = ntiles * per_tile;
+  const int per_entry = MODE == kDKV ? a.batch * a.Hkv : a.batch * a.Hq;
+  const int nunits = order.n * per_entry;
   // A unit's steps: every query tile that sees its key tile (dKV), or every key tile
   // its query tile sees (dQ), in index order.  The conditions of Eq. 2 are monotonic
   // in the other tile's index within a stream, so those tiles form one range per
   // stream, [lo0, hi0) among the clean tiles and [lo1, hi1) among the noisy ones.
   // The producer finds the ranges once per unit and publishes them with the unit.
   struct Unit {
-    int tile, b, hh, g, u0, uend, nsteps, lo0, hi0, lo1, hi1;
+    int tile, b, hh, g, chunk, nch, h_lo, h_hi, u0, uend, nsteps, lo0, hi0, lo1, hi1;
   };
   __shared__ int unit_q[4];
   __shared__ int4 unit_rng[4];
   __shared__ __align__(8) uint64_t bar_unit[4];
   auto unit_base = [&](int u, Unit& U) {
-    U.tile = order.tile[u / per_tile];
-    const int rest = static_cast<int>(u % per_tile);
-    U.b = rest / a.Hq;
-    U.hh = rest % a.Hq;  // the query head
-    U.g = U.hh / a.G;    // its KV head
+    const uint32_t e = order.entry[u / per_entry];
+    const int rest = u % per_entry;
+    U.tile = static_cast<int>(e & 0xFFFFu);
+    U.chunk = static_cast<int>((e >> 16) & 0xFFu);
+    U.nch = static_cast<int>(e >> 24);
+    if (MODE == kDKV) {  // query heads [h_lo, h_hi) of KV head g's group
+      U.b = rest / a.Hkv;
+      U.g = rest % a.Hkv;
+      U.h_lo = U.g * a.G + (U.chunk * a.G) / U.nch;
+      U.h_hi = U.g * a.G + ((U.chunk + 1) * a.G) / U.nch;
+      U.hh = U.h_lo;
+    } else {  // one query head
+      U.b = rest / a.Hq;
+      U.hh = rest % a.Hq;
+      U.g = U.hh / a.G;
+      U.h_lo = U.hh;
+      U.h_hi = U.hh + 1;
+    }
     tile_rows(a, U.tile, U.u0, U.uend);
   };
   auto set_ranges = [&](Unit& U, int lo0, int hi0, int lo1, int hi1) {
     U.lo0 = lo0, U.hi0 = hi0, U.lo1 = lo1, U.hi1 = hi1;
-    U.nsteps = (hi0 - lo0) + (hi1 - lo1);
+    U.nsteps = (U.h_hi - U.h_lo) * ((hi0 - lo0) + (hi1 - lo1));  // (head, other tile) pairs
   };
   auto scan_ranges = [&](Unit& U) {  // producer: the visible tiles of each stream
     int lo[2] = {-1, -1}, hi[2] = {0, 0};
@@ -294,6 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (o < U.lo0) o = U.lo0;
     if (o >= U.hi0 && o < U.lo1) o = U.lo1;
     return o;
+  };
+  // the unit's next step (query head h, other tile o), heads outermost; h < 0 before
+  // the first step
+  auto next_step = [&](const Unit& U, int& h, int& o) {
+    if (h < 0) {
+      h = U.h_lo;
+      o = next_other(U, -1);
+      return;
+    }
+    o = next_other(U, o);
+    if (o >= U.hi1) {
+      ++h;
+      o = next_other(U, -1);
+    }
   };
 
   if (threadIdx.x == 0) {
@@ -374,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(fixed_s + C::TILE + c * kBox, &tm_do, &bar_fixed, 64 * c, U.hh, U.u0, U.b);
           }
         }
-        for (int n = 0, ot = -1; ok && n < U.nsteps; ++n) {
-          ot = next_other(U, ot);
+        for (int n = 0, hs = -1, ot = -1; ok && n < U.nsteps; ++n) {
+          next_step(U, hs, ot);
           int o0, oe;
           tile_rows(a, ot, o0, oe);
           for (int j = 0; j < 2; ++j) {  // ring tiles of a step: dO, Q (dKV) or K, V (dQ)
@@ -388,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const CUtensorMap* tm = MODE == kDKV ? (y ? &tm_q : &tm_do) : (y ? &tm_k : &tm_v);
-            const int hc = MODE == kDKV ? U.hh : U.g;
+            const int hc = MODE == kDKV ? hs : U.g;
             const uint32_t dst = ring_s + sl * C::TILE;
             mbar_arrive_expect_tx(&bar_stage[sl], C::TILE);
             for (int c = 0; c < C::NB; ++c) tma_load_4d(dst + c * kBox, tm, &bar_stage[sl], 64 * c, hc, o0, U.b);
@@ -544,9 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit U;
     for (int ur = 0; ok && unit(ur, U); ++ur) {
       const int b = U.b, hh = U.hh, g = U.g, tile = U.tile, u0 = U.u0, uend = U.uend, nsteps = U.nsteps;
-      for (int n = 0, ot = -1; n < nsteps; ++n, ++gs) {
-        ot = next_other(U, ot);
-        const int head = hh;
+      for (int n = 0, hs = -1, ot = -1; n < nsteps; ++n, ++gs) {
+        next_step(U, hs, ot);
+        const int head = hs;
         // query tile and key tile of this step
         const int qt = MODE == kDKV ? ot : tile, kt = MODE == kDKV ? tile : ot;
         int q0, qe, k0, ke;
@@ -665,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = (SPAN * ew) / D;
         const int c_lo = (SPAN * ew) % D;
         const float f = (MODE == kDKV && m == 1) ? 1.f : a.scale;  // dV carries no scale
-        const bool fp32_out = MODE == kDKV && a.part != nullptr;  // GQA: the query head's fp32 partial
+        const bool fp32_out = MODE == kDKV && U.nch > 1;  // a chunk of a GQA group: its fp32 partial
         // The block leaves through shared memory, so that every global store writes
         // whole rows of consecutive addresses (a lane per row would scatter each store
         // instruction over 32 rows): the lane stages its row, 16-byte chunks XOR-swizzled
@@ -725,12 +770,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int grow = u0 + quad * 32 + j;
             if (grow < uend) {
               if (fp32_out) {
-                float* dst = a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + plane + grow) * a.Hq + hh) * D + c0;
+                // the chunk's slot g G + chunk of the [2][b, 2L, Hq, D] partials
+                float* dst = a.part + ((static_cast<size_t>(m) * a.batch * (2 * a.L) + plane + grow) * a.Hq +
+                                       g * a.G + U.chunk) * D + c0;
                 reinterpret_cast<uint4*>(dst)[ch] = w4;
               } else {
                 uint16_t* base = MODE == kDKV ? (m == 0 ? a.dk : a.dv) : a.dq;
                 const int H = MODE == kDKV ? a.Hkv : a.Hq;
-                const int hout = MODE == kDKV ? g : hh;  // G == 1 here in dKV mode: the query head is the KV head
+                const int hout = MODE == kDKV ? g : hh;  // dKV: one chunk covers the whole group
                 reinterpret_cast<uint4*>(base + ((plane + grow) * H + hout) * D + c0)[ch] = w4;
               }
             }
@@ -793,21 +840,51 @@ bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tiles in decreasing order of the number of tiles on the other side they meet.
-void make_order(const BwdArgs& a, int mode, UnitOrder* o) {
+// Work units heaviest first.  Weight of a tile = the tiles on the other side it
+// meets (per query head).  dKV: a tile's GQA group is split into chunks of query
+// heads so that no unit exceeds about half of an SM's share of the steps (the heavy
+// key tiles early in the clean stream are seen by most query tiles); light tiles keep
+// the whole group in one unit and need no partial.
+void make_order(const BwdArgs& a, int mode, int sms, UnitOrder* o, ChunkTable* ct) {
   const int n = 2 * a.nt;
-  std::vector<int> w(n, 0), idx(n);
+  std::vector<long long> spt(n, 0);
+  long long total = 0;
   for (int t = 0; t < n; ++t) {
-    idx[t] = t;
-    for (int u = 0; u < n; ++u) w[t] += mode == kDKV ? tile_visible(a, u, t) : tile_visible(a, t, u);
+    for (int u = 0; u < n; ++u) spt[t] += mode == kDKV ? tile_visible(a, u, t) : tile_visible(a, t, u);
+    total += spt[t];
   }
-  std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) { return w[x] > w[y]; });
-  for (int t = 0; t < n; ++t) o->tile[t] = static_cast<uint16_t>(idx[t]);
+  std::vector<int> nch(n, 1);
+  if (mode == kDKV) {
+    const long long target = std::max<long long>(1, total * a.batch * a.Hq / std::max(1, sms) / 2);
+    const int gmax = std::min(a.G, 255);
+    long long sum = 0;
+    for (int t = 0; t < n; ++t) {
+      const long long group = static_cast<long long>(a.G) * spt[t];
+      nch[t] = static_cast<int>(std::min<long long>(gmax, std::max<long long>(1, (group + target - 1) / target)));
+      sum += nch[t];
+    }
+    if (sum > kMaxEntries) std::fill(nch.begin(), nch.end(), 1);  // very long sequences: whole groups
+    for (int t = 0; t < n; ++t) ct->nch[t] = static_cast<uint8_t>(nch[t]);
+  }
+  struct Entry {
+    uint32_t code;
+    long long w;
+  };
+  std::vector<Entry> es;
+  for (int t = 0; t < n; ++t)
+    for (int c = 0; c < nch[t]; ++c) {
+      const int heads = mode == kDKV ? ((c + 1) * a.G) / nch[t] - (c * a.G) / nch[t] : 1;
+      es.push_back({static_cast<uint32_t>(t) | (static_cast<uint32_t>(c) << 16) | (static_cast<uint32_t>(nch[t]) << 24),
+                    spt[t] * heads});
+    }
+  std::stable_sort(es.begin(), es.end(), [](const Entry& x, const Entry& y) { return x.w > y.w; });
+  o->n = static_cast<int>(es.size());
+  for (int i = 0; i < o->n; ++i) o->entry[i] = es[i].code;
 }
 
 template <int D, int MODE>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-           const BwdArgs& a, cudaStream_t stream) {
+           const BwdArgs& a, const UnitOrder& order, cudaStream_t stream) {
   using C = BCfg<D, MODE>;
   static bool configured = false;
   if (!configured) {
@@ -815,11 +892,10 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
     configured = true;
   }
-  UnitOrder order;
-  make_order(a, MODE, &order);
   BwdArgs am = a;
   am.next_unit = a.next_unit + MODE;  // one counter per mode
-  const long long units = 2LL * a.nt * a.batch * a.Hq;
+  const long long units =
+      static_cast<long long>(order.n) * (MODE == kDKV ? a.batch * a.Hkv : a.batch * a.Hq);
   const int grid = static_cast<int>(std::min<long long>(units, mars_host::num_sms()));  // persistent CTAs
   cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(grid), dim3(kThreads), C::SMEM, stream);
   cudaLaunchAttribute attr[1];
@@ -892,6 +968,13 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
       !make_map(&tv, v, D, Hkv, 2 * L, batch) || !make_map(&tdo, dout, D, Hq, 2 * L, batch))
     return MARS_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = mars_host::num_sms();
+  static UnitOrder order_kv, order_q;  // large: kept off the stack (calls on one thread at a time)
+  static ChunkTable chunks;
+  static std::mutex order_mu;
+  std::lock_guard<std::mutex> lock(order_mu);
+  make_order(a, kDKV, sms, &order_kv, &chunks);
+  make_order(a, kDQ, sms, &order_q, nullptr);
   const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
   {
     cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(static_cast<int>((rows * (D / 8) + 255) / 256)), dim3(256), 0, s);
@@ -902,16 +985,16 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
                                              counters, batch, 2 * L, Hq, D);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
   }
-  rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, s);
+  rc = D == 64 ? launch<64, kDKV>(tq, tk, tv, tdo, a, order_kv, s) : launch<128, kDKV>(tq, tk, tv, tdo, a, order_kv, s);
   if (rc != MARS_OK) return rc;
   if (a.part != nullptr) {
     const long long e8 = 2LL * batch * 2 * L * Hkv * D / 8;
     cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(static_cast<int>((e8 + 255) / 256)), dim3(256), 0, s);
     cudaLaunchAttribute attr[1];
     mars_host::pdl_attr(cfg, attr);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel, static_cast<const float*>(a.part), dk, dv, batch,
-                                             2 * L, Hkv, a.G, D);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel, static_cast<const float*>(a.part), dk, dv, batch, L,
+                                             nt, Hkv, a.G, D, chunks);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
   }
-  return D == 64 ? launch<64, kDQ>(tq, tk, tv, tdo, a, s) : launch<128, kDQ>(tq, tk, tv, tdo, a, s);
+  return D == 64 ? launch<64, kDQ>(tq, tk, tv, tdo, a, order_q, s) : launch<128, kDQ>(tq, tk, tv, tdo, a, order_q, s);
 }
