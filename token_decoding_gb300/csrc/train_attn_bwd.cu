@@ -99,6 +99,9 @@ struct BCfg {
 constexpr int kMaxEntries = 4096;
 struct UnitOrder {
   uint32_t entry[kMaxEntries];
+  // per tile: its steps' other tiles, [lo0, hi0) in the clean stream and [lo1, hi1)
+  // in the noisy one (the same for every unit of the tile)
+  uint16_t rng[kMaxTiles][4];
   int n;
 };
 // Chunks per tile (dKV), for reduce_kernel: tiles with one chunk are already final.
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // its query tile sees (dQ), in index order.  The conditions of Eq. 2 are monotonic
   // in the other tile's index within a stream, so those tiles form one range per
   // stream, [lo0, hi0) among the clean tiles and [lo1, hi1) among the noisy ones.
-  // The producer finds the ranges once per unit and publishes them with the unit.
+  // The host finds the ranges once per tile; the producer publishes them with the unit.
   struct Unit {
     int tile, b, hh, g, chunk, nch, h_lo, h_hi, u0, uend, nsteps, lo0, hi0, lo1, hi1;
   };
@@ -292,19 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto set_ranges = [&](Unit& U, int lo0, int hi0, int lo1, int hi1) {
     U.lo0 = lo0, U.hi0 = hi0, U.lo1 = lo1, U.hi1 = hi1;
     U.nsteps = (U.h_hi - U.h_lo) * ((hi0 - lo0) + (hi1 - lo1));  // (head, other tile) pairs
-  };
-  auto scan_ranges = [&](Unit& U) {  // producer: the visible tiles of each stream
-    int lo[2] = {-1, -1}, hi[2] = {0, 0};
-    for (int o = 0; o < ntiles; ++o) {
-      if (MODE == kDKV ? tile_visible(a, o, U.tile) : tile_visible(a, U.tile, o)) {
-        const int st = o >= a.nt;
-        if (lo[st] < 0) lo[st] = o;
-        hi[st] = o + 1;
-      }
-    }
-    if (lo[0] < 0) lo[0] = hi[0] = 0;               // empty clean range
-    if (lo[1] < 0) lo[1] = hi[1] = ntiles;          // empty noisy range
-    set_ranges(U, lo[0], hi[0], lo[1], hi[1]);
   };
   // the r-th unit of this CTA as the consumers see it: false at the end (or on a timeout)
   auto unit = [&](int r, Unit& U) -> bool {
@@ -397,8 +387,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = r == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(a.next_unit, 1);
         if (u < nunits) {
           unit_base(u, U);
-          scan_ranges(U);
+          const uint16_t* rg = order.rng[U.tile];
+          set_ranges(U, rg[0], rg[1], rg[2], rg[3]);
           unit_rng[r & 3] = make_int4(U.lo0, U.hi0, U.lo1, U.hi1);
+          // the unit's fixed tiles toward L2 now: they load once the previous unit's
+          // last S and dP have read the current ones
+          for (int c = 0; c < C::NB; ++c) {
+            if (MODE == kDKV) {
+              tma_prefetch_l2_4d(&tm_k, 64 * c, U.g, U.u0, U.b);
+              tma_prefetch_l2_4d(&tm_v, 64 * c, U.g, U.u0, U.b);
+            } else {
+              tma_prefetch_l2_4d(&tm_q, 64 * c, U.hh, U.u0, U.b);
+              tma_prefetch_l2_4d(&tm_do, 64 * c, U.hh, U.u0, U.b);
+            }
+          }
         }
         unit_q[r & 3] = u < nunits ? u : -1;
         mbar_arrive(&bar_unit[r & 3]);  // release: the slot is written
@@ -845,12 +847,29 @@ bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch) {
 // heads so that no unit exceeds about half of an SM's share of the steps (the heavy
 // key tiles early in the clean stream are seen by most query tiles); light tiles keep
 // the whole group in one unit and need no partial.
-void make_order(const BwdArgs& a, int mode, int sms, UnitOrder* o, ChunkTable* ct) {
+bool make_order(const BwdArgs& a, int mode, int sms, UnitOrder* o, ChunkTable* ct) {
   const int n = 2 * a.nt;
   std::vector<long long> spt(n, 0);
   long long total = 0;
   for (int t = 0; t < n; ++t) {
-    for (int u = 0; u < n; ++u) spt[t] += mode == kDKV ? tile_visible(a, u, t) : tile_visible(a, t, u);
+    int lo[2] = {-1, -1}, hi[2] = {0, 0};
+    for (int u = 0; u < n; ++u) {
+      if (mode == kDKV ? tile_visible(a, u, t) : tile_visible(a, t, u)) {
+        ++spt[t];
+        const int st = u >= a.nt;
+        if (lo[st] < 0) lo[st] = u;
+        hi[st] = u + 1;
+      }
+    }
+    if (lo[0] < 0) lo[0] = hi[0] = 0;  // empty clean range
+    if (lo[1] < 0) lo[1] = hi[1] = n;  // empty noisy range
+    // the visible tiles of each stream are one range (Eq. 2 is monotonic in the tile
+    // index within a stream); the kernel relies on it
+    if (spt[t] != (hi[0] - lo[0]) + (hi[1] - lo[1])) return false;
+    o->rng[t][0] = static_cast<uint16_t>(lo[0]);
+    o->rng[t][1] = static_cast<uint16_t>(hi[0]);
+    o->rng[t][2] = static_cast<uint16_t>(lo[1]);
+    o->rng[t][3] = static_cast<uint16_t>(hi[1]);
     total += spt[t];
   }
   std::vector<int> nch(n, 1);
@@ -880,6 +899,7 @@ void make_order(const BwdArgs& a, int mode, int sms, UnitOrder* o, ChunkTable* c
   std::stable_sort(es.begin(), es.end(), [](const Entry& x, const Entry& y) { return x.w > y.w; });
   o->n = static_cast<int>(es.size());
   for (int i = 0; i < o->n; ++i) o->entry[i] = es[i].code;
+  return true;
 }
 
 template <int D, int MODE>
@@ -973,8 +993,8 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
   static ChunkTable chunks;
   static std::mutex order_mu;
   std::lock_guard<std::mutex> lock(order_mu);
-  make_order(a, kDKV, sms, &order_kv, &chunks);
-  make_order(a, kDQ, sms, &order_q, nullptr);
+  if (!make_order(a, kDKV, sms, &order_kv, &chunks) || !make_order(a, kDQ, sms, &order_q, nullptr))
+    return MARS_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
   {
     cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(static_cast<int>((rows * (D / 8) + 255) / 256)), dim3(256), 0, s);
