@@ -111,11 +111,12 @@ int mars_train_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  *   lse        [batch, Hq, 2L] fp32 (the forward's, natural log)
  *   workspace  device buffer of >= mars_train_attn_bwd_workspace_size(batch,
  *              L, Hq, Hkv, D) bytes (it holds rowsum(dO * o), two work counters
- *              and, when Hq > Hkv, each query head's fp32 dK, dV before the group
- *              sum); contents on entry do not matter; calls that share it must
- *              not overlap in time.
- * Kernel launches on `stream`: the row sums, dK and dV per (query head, key
- * tile), the sum over each GQA group (when Hq > Hkv), then dQ per query tile.
+ *              and, when Hq > Hkv, fp32 dK, dV partials of the GQA groups that
+ *              are split into chunks of query heads); contents on entry do not
+ *              matter; calls that share it must not overlap in time.
+ * Kernel launches on `stream`: the row sums; dK and dV per (KV head, key tile,
+ * chunk of the group's query heads); the sum of the chunks where a group was
+ * split (when Hq > Hkv); then dQ per (query head, query tile).
  * Persistent CTAs take work units from an atomic counter, but every output
  * element comes from one fixed sequence of operations whichever CTA runs it, so
  * the result is deterministic.  Supported: D in {64, 128}; Hq % Hkv == 0; 1 <= B;

@@ -9,20 +9,23 @@
 //   dQ = scale dS k,  dK = scale dS^T q,
 // and P is recomputed from the forward's log-sum-exp: P = exp(S - lse).
 //
-// sm_103a design (tensor-bound).  Three launches, deterministic (the only atomic
+// sm_103a design (tensor-bound).  Four launches, deterministic (the only atomic
 // hands out work units):
 //   1. delta_kernel: delta_i = rowsum(dO_i * O_i), fp32, 16-byte loads.
-//   2. bwd_kernel<kDKV>: one unit per (sequence, query head, 128-key tile).  For
-//      every 128-row query tile that sees the key tile (an exact interval test
-//      on Eq. 2's structure) tcgen05 computes dP = dO V^T and S = Q K^T into
+//   2. bwd_kernel<kDKV>: one unit per (sequence, KV head, 128-key tile, chunk of
+//      the group's query heads).  For every query head of the chunk and every
+//      128-row query tile that sees the key tile (an exact interval test on
+//      Eq. 2's structure) tcgen05 computes dP = dO V^T and S = Q K^T into
 //      tensor memory; the elementwise warps form P and dS and write them to
 //      shared memory as SW128 [128 rows x 64 keys] tiles; tcgen05 then
 //      accumulates dV += P^T dO and dK += dS^T Q in tensor memory (P / dS read
-//      MN-major as the A operand, Q / dO MN-major as B).  With GQA each query
-//      head's dK, dV go to an fp32 partial in the workspace and reduce_kernel
-//      sums the heads of a group in a fixed order (one unit per head keeps the
-//      heaviest key tile from serialising a whole group's work).
-//   3. bwd_kernel<kDQ>: one unit per (sequence, query head, 128-row query tile):
+//      MN-major as the A operand, Q / dO MN-major as B) over the whole chunk.
+//      A group is split into chunks only on the heavy key tiles (so that no unit
+//      serialises a large share of the work on one SM); a one-chunk unit writes
+//      bf16 dK, dV directly, a split one an fp32 partial per chunk.
+//   3. reduce_kernel (GQA): the chunks' partials of the split tiles, summed in
+//      chunk order.
+//   4. bwd_kernel<kDQ>: one unit per (sequence, query head, 128-row query tile):
 //      the same dP, S, dS for every key tile the query tile sees, then
 //      dQ += dS K (dS K-major, K MN-major).
 // CTAs are persistent (one per SM) and take units heaviest first from a work
@@ -96,14 +99,20 @@ struct BCfg {
 // chunk's query heads (one chunk: the whole group, written as bf16 directly; more:
 // an fp32 partial per chunk, summed by reduce_kernel).  dQ: entry x (batch, query
 // head) units, one chunk each.
+// The order is a kernel parameter, copied with every launch, so a small one (3 KB)
+// is used when the entries and tiles fit (each KB of parameter delays the launch).
 constexpr int kMaxEntries = 4096;
-struct UnitOrder {
-  uint32_t entry[kMaxEntries];
+constexpr int kSmallEntries = 512, kSmallTiles = 128;
+template <int NE, int NT>
+struct UnitOrderT {
+  uint32_t entry[NE];
   // per tile: its steps' other tiles, [lo0, hi0) in the clean stream and [lo1, hi1)
   // in the noisy one (the same for every unit of the tile)
-  uint16_t rng[kMaxTiles][4];
+  uint16_t rng[NT][4];
   int n;
 };
+using UnitOrder = UnitOrderT<kMaxEntries, kMaxTiles>;
+using SmallOrder = UnitOrderT<kSmallEntries, kSmallTiles>;
 // Chunks per tile (dKV), for reduce_kernel: tiles with one chunk are already final.
 struct ChunkTable {
   uint8_t nch[kMaxTiles];
@@ -235,11 +244,11 @@ __global__ void __launch_bounds__(256) reduce_kernel(const float* __restrict__ p
 }
 
 // ---------------------------------------------------------------- main kernel
-template <int D, int MODE>
+template <int D, int MODE, int NE, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdArgs a,
-               const __grid_constant__ UnitOrder order) {
+               const __grid_constant__ UnitOrderT<NE, NT> order) {
   using C = BCfg<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -906,9 +915,12 @@ template <int D, int MODE>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
            const BwdArgs& a, const UnitOrder& order, cudaStream_t stream) {
   using C = BCfg<D, MODE>;
+  auto big = bwd_kernel<D, MODE, kMaxEntries, kMaxTiles>;
+  auto small = bwd_kernel<D, MODE, kSmallEntries, kSmallTiles>;
   static bool configured = false;
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(big, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(small, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return mars_host::cuda_fail(e);
     configured = true;
   }
@@ -920,7 +932,16 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
   cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(grid), dim3(kThreads), C::SMEM, stream);
   cudaLaunchAttribute attr[1];
   mars_host::pdl_attr(cfg, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_kernel<D, MODE>, tq, tk, tv, tdo, am, order);
+  cudaError_t e;
+  if (order.n <= kSmallEntries && 2 * a.nt <= kSmallTiles) {
+    static SmallOrder so;  // filled and copied under the caller's lock
+    std::copy(order.entry, order.entry + order.n, so.entry);
+    for (int t = 0; t < 2 * a.nt; ++t) std::copy(order.rng[t], order.rng[t] + 4, so.rng[t]);
+    so.n = order.n;
+    e = cudaLaunchKernelEx(&cfg, small, tq, tk, tv, tdo, am, so);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, big, tq, tk, tv, tdo, am, order);
+  }
   return e == cudaSuccess ? MARS_OK : mars_host::cuda_fail(e);
 }
 
