@@ -105,9 +105,13 @@ def test_qwen05b_shape_every_group():
     _shape_groups(s, 3500, [(b, g) for b in range(s.batch) for g in range(s.Hkv)])
 
 
-def test_qwen7b_shape_two_groups():
+def test_qwen7b_shape_every_group():
+    """Every (sequence, KV group) of the 7B shape.  Its dK/dV units split a group's
+    seven query heads into 1 to 5 chunks depending on the key tile (5 for the first
+    clean tile, 1 from the 14th and for every noisy one), so uneven chunks, whole
+    groups written directly and the chunk reduction all meet the oracle here."""
     s = synth.TRAIN_7B
-    _shape_groups(s, 3600, [(0, 0), (1, 2)])
+    _shape_groups(s, 3600, [(b, g) for b in range(s.batch) for g in range(s.Hkv)])
 
 
 def test_deterministic():
