@@ -266,7 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ahead of the elementwise warps (it fetches unit r + 2 only after unit r's last
   // S, which comes after the elementwise warps' P of unit r - 1), so four slots
   // suffice.
-  const int ntiles = 2 * a.nt;
   const int per_entry = MODE == kDKV ? a.batch * a.Hkv : a.batch * a.Hq;
   const int nunits = order.n * per_entry;
   // A unit's steps: every query tile that sees its key tile (dKV), or every key tile
