@@ -14,7 +14,7 @@ kernel's working set exceeds twice the L2, so nothing is served from a warm L2
 between iterations.  The decode kernels' own rates come from graphs of
 back-to-back launches of one kernel.
 
---impl reference times the fp64 CPU oracle (the reference arm of this build)
+--impl reference times the fp64 CPU oracle (the reference arm: the plain CPU implementation)
 on bounded samples of the same workload.
 """
 

@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
 module.  The CUDA library never calls it, and it shares no code, header,
 table or helper with the CUDA path: it is written directly from the method's
-definition so that it can judge the kernels.
+definition so that it can check the kernels.
 
 Sources (cited by page title and section / equation):
 
