@@ -557,6 +557,87 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // visible columns of this row inside the tile: [vlo, vhi] (empty when vlo > vhi)
         const int vlo = part ? max((nz ? n_lo_v : 0) - kstart, 0) : 0;
         const int vhi = part ? min((nz ? n_hi_v : c_hi_v) - kstart, kBN - 1) : kBN - 1;
+        if constexpr (C::SEPP) {
+          // The noisy tile of the query tile's own blocks (its last tile, at L + 128 j):
+          // row r sees only the keys [B floor(r / B), r] of the tile, at most B of them,
+          // and when B divides 32 they all lie in the row's warp's own 32 columns.  Only
+          // those 32 scores are read, masked and exponentiated; the other 96 columns of
+          // P are stored as zeros.  (Not on split tiles: j = 0 keeps the hi + lo P.)
+          const bool self_tile = it.noisy_q && it.j > 0 && n == nt - 1 && (32 % a.B) == 0 &&
+                                 kstart == a.L + kBM * it.j;
+          if (self_tile) {
+            uint32_t v[32];
+            tmem_ld32(s_col + 32 * quad, v);
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar_sfree[x]);  // S_x is in registers: the next S may overwrite it
+            {
+              const int lo = min(max(vlo - 32 * quad, 0), 32), hi = min(max(vhi - 32 * quad + 1, 0), 32);
+              const uint32_t below_hi = hi >= 32 ? 0xffffffffu : (1u << hi) - 1u;
+              const uint32_t below_lo = lo >= 32 ? 0xffffffffu : (1u << lo) - 1u;
+              const uint32_t msk = below_hi & ~below_lo;
+#pragma unroll
+              for (int c = 0; c < 32; ++c) v[c] = ((msk >> c) & 1u) ? v[c] : 0xFF800000u;
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              mx0 = fmax3(mx0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+              mx1 = fmax3(mx1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            }
+            const float tmax = fmaxf(mx0, mx1) * a.scale_log2;
+            float alpha = 1.f;
+            const bool grow = tmax > m_used + kRescaleThreshold;
+            if (grow) {
+              alpha = fast_exp2(m_used - tmax);  // 0 when m_used is -inf
+              m_used = tmax;
+            }
+            const float neg_mu = m_used == -INFINITY ? 0.f : -m_used;
+            uint64_t sum2x = 0;
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float x0, x1;
+              fma2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), a.scale_log2, neg_mu, x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(sum2x, p0, p1);
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            if (cpw > 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&bar_pfree[x], (cpw - 1) & 1));
+              if (!ok) break;
+            }
+            tc_fence_after();
+            if (n > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+              for (int c = 0; c < D; c += 16) {
+                uint32_t ov[16];
+                tmem_ld16(o_col + c, ov);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                tmem_st16(o_col + c, ov);
+              }
+            }
+            const uint32_t p_col = tmem + lane_addr + C::P_COL + x * (kBN / 2);
+            uint32_t zero[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) zero[e] = 0u;
+#pragma unroll
+            for (int q = 0; q < kBN / 32; ++q) {  // keys [32 q, 32 q + 32) -> columns [16 q, 16 q + 16)
+              if (q == quad)
+                tmem_st16(p_col + 16 * q, pk);
+              else
+                tmem_st16(p_col + 16 * q, zero);
+            }
+            l = l * alpha + sum2(sum2x);
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar_p[x]);
+            ++cpw;
+            continue;
+          }
+        }
         // One pass: the row's 128 scores are read from tensor memory once and kept in
         // registers for the max and then exp2 and the bf16 store of P.  Hidden scores
         // become -inf (exp2 of them is exactly 0).
