@@ -54,6 +54,14 @@ def test_several_tiles_and_ragged_ends(L, B, D):
     case(2, L, B, 4, 2, D, 10 * L + B)
 
 
+@pytest.mark.parametrize("L,B", [(300, 1), (300, 2), (257, 16), (384, 32), (200, 8)])
+def test_own_block_tile_d64(L, B):
+    """Block sizes that divide 32 with several query tiles at D = 64: the noisy query
+    tiles after the first take the own-block path (only the warp's 32 columns of
+    their last key tile are read); ragged last tiles included."""
+    case(2, L, B, 6, 2, 64, 13 * L + B)
+
+
 @pytest.mark.parametrize("L,B", [(10, 16), (100, 100), (129, 128), (260, 200), (128, 128), (1, 1), (5, 2)])
 def test_degenerate_blocks(L, B):
     case(1, L, B, 2, 1, 64, 7 * L + B)
