@@ -639,17 +639,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           }
         }
         // One pass: the row's 128 scores are read from tensor memory once and kept in
-        // registers for the max and then exp2 and the bf16 store of P.  Hidden scores
-        // become -inf (exp2 of them is exactly 0).
+        // registers for the max and then exp2 and the bf16 store of P.  An unmasked tile
+        // reads them with the reducing load, which also returns each 32 columns' maximum;
+        // a masked tile turns hidden scores into -inf (exp2 of them is exactly 0) and
+        // takes the maximum after that.
         uint32_t v0[kBN];
+        float gmax[kBN / 32];
+        if (!part) {
 #pragma unroll
-        for (int c = 0; c < kBN; c += 32) tmem_ld32(s_col + c, *reinterpret_cast<uint32_t(*)[32]>(&v0[c]));
+          for (int c = 0; c < kBN; c += 32)
+            gmax[c / 32] = tmem_ld32_max(s_col + c, *reinterpret_cast<uint32_t(*)[32]>(&v0[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; c += 32) tmem_ld32(s_col + c, *reinterpret_cast<uint32_t(*)[32]>(&v0[c]));
+        }
         tc_wait_ld();
         if constexpr (C::SEPP) {
           tc_fence_before();
           mbar_arrive(&bar_sfree[x]);  // S_x is in registers: the next S may overwrite it
         }
-        if (part) {
+        float tile_max;
+        if (!part) {
+          static_assert(kBN == 128, "four reducing loads per tile");
+          tile_max = fmaxf(fmaxf(gmax[0], gmax[1]), fmaxf(gmax[2], gmax[3])) * a.scale_log2;
+        } else {
           // the row's visible columns as one bit mask per 32 columns, then one bit
           // test and select per score (cheaper than two compares per score)
 #pragma unroll
@@ -661,16 +674,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) v0[32 * q + c] = ((m >> c) & 1u) ? v0[32 * q + c] : 0xFF800000u;
           }
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 8) {
-          mx0 = fmax3(mx0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(v0[c + 2]), __uint_as_float(v0[c + 3]));
-          mx2 = fmax3(mx2, __uint_as_float(v0[c + 4]), __uint_as_float(v0[c + 5]));
-          mx3 = fmax3(mx3, __uint_as_float(v0[c + 6]), __uint_as_float(v0[c + 7]));
+          for (int c = 0; c < kBN; c += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(v0[c + 2]), __uint_as_float(v0[c + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(v0[c + 4]), __uint_as_float(v0[c + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(v0[c + 6]), __uint_as_float(v0[c + 7]));
+          }
+          tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
         }
-        const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;
         // lazy rescale: keep the old reference max unless the new one is 2^8 larger.
         // PV_x(n-1) is complete here: S_x(n) was issued after it and its commit covers it.
         float alpha = 1.f;
