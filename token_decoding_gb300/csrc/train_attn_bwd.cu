@@ -40,7 +40,10 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <climits>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "common.cuh"
@@ -850,11 +853,44 @@ bool make_map(CUtensorMap* m, const void* ptr, int D, int H, int n, int batch) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+struct OrderEntry {
+  uint32_t code;  // tile | chunk << 16 | chunks << 24
+  long long w;    // steps of one unit
+};
+
+// Cost, in steps, of the work a unit does besides its steps (the fixed tiles, the first
+// products, the epilogue), and the extra for writing an fp32 partial instead of bf16.
+constexpr long long kUnitCost = 2, kPartCost = 1;
+
+// Steps until the last CTA of the dK/dV pass finishes when the persistent CTAs take
+// the units in order, each as soon as it is free (each entry stands for per_entry units
+// of equal weight).
+long long makespan(const std::vector<OrderEntry>& es, long long per_entry, int sms) {
+  std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
+  const long long units = static_cast<long long>(es.size()) * per_entry;
+  for (long long i = 0; i < std::min<long long>(std::max(1, sms), units); ++i) free_at.push(0);
+  long long end = 0;
+  for (const OrderEntry& e : es) {
+    const long long cost = e.w + kUnitCost + ((e.code >> 24) > 1 ? kPartCost : 0);
+    for (long long u = 0; u < per_entry; ++u) {
+      const long long t = free_at.top() + cost;
+      free_at.pop();
+      free_at.push(t);
+      end = std::max(end, t);
+    }
+  }
+  return end;
+}
+
 // Work units heaviest first.  Weight of a tile = the tiles on the other side it
 // meets (per query head).  dKV: a tile's GQA group is split into chunks of query
-// heads so that no unit exceeds about half of an SM's share of the steps (the heavy
-// key tiles early in the clean stream are seen by most query tiles); light tiles keep
-// the whole group in one unit and need no partial.
+// heads, because the heavy key tiles early in the clean stream are seen by most query
+// tiles and a whole group in one unit would serialise on one SM; light tiles keep the
+// whole group in one unit and need no partial.  A unit may hold at most a target
+// number of steps, SM share / d for d in {1, 1.25, 1.5, 2, 2.5, 3, 4}; the chunking
+// kept is the one whose heaviest-first schedule ends first (makespan), the fewest
+// chunks on a tie.  The finishing time moves in steps as the chunk counts change,
+// so no single d suits every shape.
 bool make_order(const BwdArgs& a, int mode, int sms, UnitOrder* o, ChunkTable* ct) {
   const int n = 2 * a.nt;
   std::vector<long long> spt(n, 0);
@@ -880,31 +916,43 @@ bool make_order(const BwdArgs& a, int mode, int sms, UnitOrder* o, ChunkTable* c
     o->rng[t][3] = static_cast<uint16_t>(hi[1]);
     total += spt[t];
   }
+  auto build = [&](const std::vector<int>& nch, std::vector<OrderEntry>& es) {
+    es.clear();
+    for (int t = 0; t < n; ++t)
+      for (int c = 0; c < nch[t]; ++c) {
+        const int heads = mode == kDKV ? ((c + 1) * a.G) / nch[t] - (c * a.G) / nch[t] : 1;
+        es.push_back({static_cast<uint32_t>(t) | (static_cast<uint32_t>(c) << 16) |
+                          (static_cast<uint32_t>(nch[t]) << 24),
+                      spt[t] * heads});
+      }
+    std::stable_sort(es.begin(), es.end(), [](const OrderEntry& x, const OrderEntry& y) { return x.w > y.w; });
+  };
   std::vector<int> nch(n, 1);
+  std::vector<OrderEntry> es;
   if (mode == kDKV) {
-    const long long target = std::max<long long>(1, total * a.batch * a.Hq / std::max(1, sms) / 2);
+    const double share = static_cast<double>(total) * a.batch * a.Hq / std::max(1, sms);  // steps per SM
     const int gmax = std::min(a.G, 255);
-    long long sum = 0;
-    for (int t = 0; t < n; ++t) {
-      const long long group = static_cast<long long>(a.G) * spt[t];
-      nch[t] = static_cast<int>(std::min<long long>(gmax, std::max<long long>(1, (group + target - 1) / target)));
-      sum += nch[t];
+    std::vector<int> cand(n);
+    long long best = LLONG_MAX;
+    for (const double d : {1.0, 1.25, 1.5, 2.0, 2.5, 3.0, 4.0}) {
+      const long long target = std::max<long long>(1, static_cast<long long>(share / d));
+      long long sum = 0;
+      for (int t = 0; t < n; ++t) {
+        const long long group = static_cast<long long>(a.G) * spt[t];
+        cand[t] = static_cast<int>(std::min<long long>(gmax, std::max<long long>(1, (group + target - 1) / target)));
+        sum += cand[t];
+      }
+      if (sum > kMaxEntries) std::fill(cand.begin(), cand.end(), 1);  // very long sequences: whole groups
+      build(cand, es);
+      const long long m = makespan(es, static_cast<long long>(a.batch) * a.Hkv, sms);
+      if (m < best) {
+        best = m;
+        nch = cand;
+      }
     }
-    if (sum > kMaxEntries) std::fill(nch.begin(), nch.end(), 1);  // very long sequences: whole groups
     for (int t = 0; t < n; ++t) ct->nch[t] = static_cast<uint8_t>(nch[t]);
   }
-  struct Entry {
-    uint32_t code;
-    long long w;
-  };
-  std::vector<Entry> es;
-  for (int t = 0; t < n; ++t)
-    for (int c = 0; c < nch[t]; ++c) {
-      const int heads = mode == kDKV ? ((c + 1) * a.G) / nch[t] - (c * a.G) / nch[t] : 1;
-      es.push_back({static_cast<uint32_t>(t) | (static_cast<uint32_t>(c) << 16) | (static_cast<uint32_t>(nch[t]) << 24),
-                    spt[t] * heads});
-    }
-  std::stable_sort(es.begin(), es.end(), [](const Entry& x, const Entry& y) { return x.w > y.w; });
+  build(nch, es);
   o->n = static_cast<int>(es.size());
   for (int i = 0; i < o->n; ++i) o->entry[i] = es[i].code;
   return true;
@@ -1009,12 +1057,19 @@ extern "C" int mars_train_attn_bwd(const uint16_t* q, const uint16_t* k, const u
     return MARS_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int sms = mars_host::num_sms();
+  // The orders depend only on the shape: the last shape's are kept.
   static UnitOrder order_kv, order_q;  // large: kept off the stack (calls on one thread at a time)
   static ChunkTable chunks;
+  static int last_key[6] = {0, 0, 0, 0, 0, 0};
   static std::mutex order_mu;
   std::lock_guard<std::mutex> lock(order_mu);
-  if (!make_order(a, kDKV, sms, &order_kv, &chunks) || !make_order(a, kDQ, sms, &order_q, nullptr))
-    return MARS_ERR_INVALID_ARG;
+  const int key[6] = {batch, L, B, Hq, Hkv, sms};
+  if (!std::equal(key, key + 6, last_key)) {
+    std::fill(last_key, last_key + 6, 0);
+    if (!make_order(a, kDKV, sms, &order_kv, &chunks) || !make_order(a, kDQ, sms, &order_q, nullptr))
+      return MARS_ERR_INVALID_ARG;
+    std::copy(key, key + 6, last_key);
+  }
   const long long rows = static_cast<long long>(batch) * 2 * L * Hq;
   {
     cudaLaunchConfig_t cfg = mars_host::pdl_config(dim3(static_cast<int>((rows * (D / 8) + 255) / 256)), dim3(256), 0, s);
