@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_wmerge[C::IN_SLOTS];  // small-unit merge weights, [rows_per][C]
   __shared__ uint32_t tmem_slot;
   __shared__ int s_b;
-  __shared__ float s_mstate[2][kRows], s_lstate[2][kRows];  // single-CTA units: each stream's (m, l) per row
+  __shared__ float s_mstate[2][kRows], s_lstate[2][kRows];  // each stream's (m, l) per row (one-CTA and small units)
   __shared__ int s_len[kSortLimit];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -220,6 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // launched as a programmatic dependent: nothing global is read before the previous
   // kernel in the stream has completed
   griddep_wait();
+  // The next kernel may start its set-up now, on the SMs this grid leaves free (a
+  // small batch uses few); it reads nothing this kernel writes before its own wait.
+  griddep_launch_dependents();
 
   // ---- which sequence: heavy-first rank order (stable by index) or plain order
   const int b_rank = unit_rank / units_per_b;
@@ -552,46 +555,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && nmine > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar_o[x], 0));
     if (!ok && lane == 0) set_status(a.status, MARS_DEV_TIMEOUT);
     const bool have = ok && nmine > 0;
-    // ---- combine this CTA's 8 states of each row (state w = 4 x + q) through shared
-    // memory; warp w then writes columns [w D / 8, (w + 1) D / 8) of every combined
-    // row, and warp 0 the row's (m, l), into the outbox [32][D + 4]
+    // ---- combine this CTA's 8 states of each row (stream x, lane quarter q), in two
+    // levels.  The warps of streams A and B in quarter q reach the same tensor-memory
+    // lanes, so each first merges the two streams' O of its rows from tensor memory,
+    // warp (x, q) columns [x D / 2, (x + 1) D / 2), with weights from the exchanged
+    // (m, l), and writes the quarter's state to shared memory; then warp w = 4 x + q
+    // merges columns [w D / 8, (w + 1) D / 8) of the four quarter states of every row
+    // into the outbox [32][D + 4], and warp 0 adds the row's (m, l).
     const int wst = x * 4 + q;
+    // each stream's (m, l) of the rows, exchanged outside the ring (the other stream's
+    // products may still read the ring until the barrier below)
+    s_mstate[x][q * 32 + r] = have ? m_used : -INFINITY;
+    s_lstate[x][q * 32 + r] = have ? l : 0.f;
     named_bar_sync(1, 256);  // every product of both streams is complete: the ring is free
     tc_fence_after();
-    float* xo = reinterpret_cast<float*>(smem + C::RING_OFF);  // [8][32][D], 16-byte units XOR (row & 7)
-    float* xm = xo + 8 * 32 * D;                               // [8][32]
-    float* xl = xm + 8 * 32;                                   // [8][32]
+    float* xo = reinterpret_cast<float*>(smem + C::RING_OFF);  // [4][32][D] used, 16-byte units XOR (row & 7)
+    float* xm = xo + 8 * 32 * D;                               // [4][32] used: the quarters' m
+    float* xl = xm + 8 * 32;                                   // [4][32] used: the quarters' l
     float* outbox = xl + 8 * 32;                               // [32][D + 4]
     {
-      float4* dst = reinterpret_cast<float4*>(xo + (wst * 32 + r) * D);
+      const float mx_ = s_mstate[x][q * 32 + r], my = s_mstate[1 - x][q * 32 + r];
+      const float mq = fmaxf(mx_, my);
+      // weights of this stream (x) and the other (y); a stream without keys weighs 0
+      // and its accumulator (never written when it had no tile) is not read into the sum
+      const float wx = mx_ == -INFINITY ? 0.f : fast_exp2(mx_ - mq);
+      const float wy = my == -INFINITY ? 0.f : fast_exp2(my - mq);
+      const uint32_t ox_col = o_col, oy_col = tmem + lane_addr + C::O_COL + (1 - x) * D;
+      float4* dst = reinterpret_cast<float4*>(xo + (q * 32 + r) * D);
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32(o_col + c, ov);
+      for (int c = x * (D / 2); c < (x + 1) * (D / 2); c += 32) {
+        uint32_t vx[32], vy[32];
+        tmem_ld32(ox_col + c, vx);
+        tmem_ld32(oy_col + c, vy);
         tc_wait_ld();
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float4 v = have ? make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                              __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 v;
+          v.x = (wx > 0.f ? wx * __uint_as_float(vx[4 * e]) : 0.f) + (wy > 0.f ? wy * __uint_as_float(vy[4 * e]) : 0.f);
+          v.y = (wx > 0.f ? wx * __uint_as_float(vx[4 * e + 1]) : 0.f) +
+                (wy > 0.f ? wy * __uint_as_float(vy[4 * e + 1]) : 0.f);
+          v.z = (wx > 0.f ? wx * __uint_as_float(vx[4 * e + 2]) : 0.f) +
+                (wy > 0.f ? wy * __uint_as_float(vy[4 * e + 2]) : 0.f);
+          v.w = (wx > 0.f ? wx * __uint_as_float(vx[4 * e + 3]) : 0.f) +
+                (wy > 0.f ? wy * __uint_as_float(vy[4 * e + 3]) : 0.f);
           dst[((c >> 2) + e) ^ (r & 7)] = v;
         }
       }
-      xm[wst * 32 + r] = have ? m_used : -INFINITY;
-      xl[wst * 32 + r] = have ? l : 0.f;
+      if (x == 0) {  // the quarter's state: max mq, sum of the weighted l
+        xm[q * 32 + r] = mq;
+        xl[q * 32 + r] = wx * s_lstate[0][q * 32 + r] + wy * s_lstate[1][q * 32 + r];
+      }
     }
     named_bar_sync(1, 256);
     if (r < R) {
-      float ws[8];
+      float ws[4];
       float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
+      for (int t = 0; t < 4; ++t) {
         ws[t] = xm[t * 32 + r];
         mx = fmaxf(mx, ws[t]);
       }
       float lsum = 0.f;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
+      for (int t = 0; t < 4; ++t) {
         ws[t] = ws[t] == -INFINITY ? 0.f : fast_exp2(ws[t] - mx);  // states without keys weigh 0
         lsum += ws[t] * xl[t * 32 + r];
       }
@@ -602,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c4 = wst * (D / 32) + j;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < 4; ++t) {
           const float4 v = x4[(t * 32 + r) * (D / 4) + (c4 ^ (r & 7))];
           acc.x += ws[t] * v.x;
           acc.y += ws[t] * v.y;
@@ -813,15 +839,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each owning CTA (rows [o rows_per, (o + 1) rows_per)) receives this CTA's combined
     // rows as one bulk copy into block `crank` of its inbox, completing on its bar_in.
     cluster_wait();  // every CTA of the cluster has started and armed its inbox
-    if (warp == 2 && lane == 0) {
+    // Lane o of warp 2 sends owner o its rows, so the copies are issued side by side
+    // (C <= 32); each lane later waits for its own copy's reads.
+    if (warp == 2 && lane < a.C) {
       const uint32_t ob = smem_u32(smem + C::RING_OFF) + 8 * 32 * D * 4 + 2 * 8 * 32 * 4;
       const uint32_t inbox = smem_u32(smem + C::INBOX_OFF) + crank * rows_per * C::ROWB;
-      for (int o = 0; o < a.C; ++o) {
-        const int n_o = min(rows_per, R - o * rows_per);
-        if (n_o <= 0) continue;
+      const int o = lane;
+      const int n_o = min(rows_per, R - o * rows_per);
+      if (n_o > 0)
         bulk_s2s_cluster(dsmem_map(inbox, o), ob + o * rows_per * C::ROWB, n_o * C::ROWB,
                          dsmem_map(smem_u32(&bar_in), o));
-      }
       bulk_commit_group();
     }
     // Finish the owned rows from the inbox: one weight per (row, source),
@@ -850,19 +877,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = r / a.Gc, hl = r % a.Gc;
         if (hl >= heads) continue;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < a.C; ++c) {
-          const float w = s_wmerge[rr * a.C + c];
-          const float4 v = reinterpret_cast<const float4*>(in + (c * rows_per + rr) * (D + 4))[d4];
-          o.x += w * v.x;
-          o.y += w * v.y;
-          o.z += w * v.z;
-          o.w += w * v.w;
+#pragma unroll
+        for (int c = 0; c < kWideCluster; ++c) {  // unrolled: the sources' loads issue together
+          if (c < a.C) {
+            const float w = s_wmerge[rr * a.C + c];
+            const float4 v = reinterpret_cast<const float4*>(in + (c * rows_per + rr) * (D + 4))[d4];
+            o.x += w * v.x;
+            o.y += w * v.y;
+            o.z += w * v.z;
+            o.w += w * v.w;
+          }
         }
         uint16_t* dst = a.o + ((static_cast<size_t>(b) * a.S + i) * a.Hq + h0 + hl) * D + 4 * d4;
         *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
       }
     }
-    if (warp == 2 && lane == 0) bulk_wait_read_all();  // the outbox has been read: this CTA may exit
+    if (warp == 2 && lane < a.C) bulk_wait_read_all();  // the outbox has been read: this CTA may exit
     __syncthreads();  // every tensor-memory read of the epilogue is done
   } else if (a.C > 1) {
     cluster_sync();
@@ -925,7 +955,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     __syncthreads();  // every tensor-memory read of the epilogue is done
   }
-  griddep_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
