@@ -1,5 +1,6 @@
 // accept.cu - mars_accept: top-1 probability, greedy token, left-to-right
-// commit with threshold tau, and the block-level KV append, in one launch.
+// commit with threshold tau, and the block-level KV append, in one call (a
+// streaming launch and a finish launch).
 //
 // Method: the authors' MARS blog post, "Inference: a knob, not a mode switch"
 // (commit while the top-1 probability holds, stop at the first position below

@@ -12,11 +12,14 @@
 //     Its query rows are (position i, head) pairs, row = i * Gc + head, at most
 //     128, so one K/V stream serves every head that shares the KV head (GQA).
 //     The rows form the M = 128 side of tcgen05.mma; rows past Gc * B are zero.
-//   * A unit is processed by a cluster of C CTAs; CTA rank c takes the c-th
-//     contiguous share of the unit's 64-key cache tiles, and the last rank also
-//     takes the tile of this step's B new keys (N = 16, rows >= B zero).  At
-//     the end the per-row softmax states of all CTAs are merged through
-//     distributed shared memory: no split-K partials reach global memory.
+//   * A unit is processed by a cluster of C CTAs; CTA rank c takes the unit's
+//     64-key cache tiles c, c + C, c + 2C, ... (known before cache_len is read),
+//     and the last rank also takes the tile of this step's B new keys (N = 16,
+//     rows >= B zero).  At the end the per-row softmax states of all CTAs are
+//     merged through distributed shared memory: no split-K partials reach global
+//     memory.  Small units (<= 32 rows, e.g. batch 1) split each tile four ways by
+//     keys over the four lane quarters and send each owning CTA its rows with one
+//     bulk copy into that CTA's inbox.
 //   * Inside a CTA the local tiles alternate between two streams A and B, each
 //     with its own S and O in tensor memory and its own online softmax, so the
 //     tensor pipe computes one stream's products while the other's softmax runs:
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp (x, q) columns [x D / 2, (x + 1) D / 2), with weights from the exchanged
     // (m, l), and writes the quarter's state to shared memory; then warp w = 4 x + q
     // merges columns [w D / 8, (w + 1) D / 8) of the four quarter states of every row
-    // into the outbox [32][D + 4], and warp 0 adds the row's (m, l).
+    // into the outbox [32][D + 4]; the warp of slice 0 adds the row's (m, l).
     const int wst = x * 4 + q;
     // each stream's (m, l) of the rows, exchanged outside the ring (the other stream's
     // products may still read the ring until the barrier below)

@@ -12,12 +12,13 @@
 //   noisy row t = i-L:  clean [0, B*floor(t/B) - 1]  and  noisy [L + B*floor(t/B), i]
 // so a 128-row query tile (always inside one stream) only visits the key
 // tiles that intersect those intervals: fully masked tiles are never loaded,
-// tiles inside every row's interval take no mask, and the rest take a
-// two-compare interval mask.
+// tiles inside every row's interval take no mask, and the rest take the row's
+// interval as one bit mask per 32 columns (one bit test per score).
 //
 // sm_103a design.  A work item is one 128-row query tile of one or two query
-// heads that share a KV head (so both read the same K/V tiles); items are
-// taken heaviest first by persistent CTAs (one per SM).
+// heads that share a KV head (so both read the same K/V tiles); a host-side
+// plan (longest first by a fitted cost model, then moves between CTAs) gives
+// each persistent CTA (one per SM) its list of items.
 //   warp 0      TMA producer: the item's Q tiles, then K and V tiles (SW128,
 //               64-column boxes) into an NS-stage ring (full/empty mbarriers).
 //   warp 1      TMEM owner and MMA issuer (one thread).  At D = 128 it issues
@@ -35,8 +36,10 @@
 //               other's softmax (the issuing warps' own latency per wait and
 //               issue was the step limit with one issuer).
 //   warps 2..5  softmax warpgroup A, warps 6..9 warpgroup B (thread = query
-//               row = TMEM lane): S from TMEM, mask, row max, exp2; P is
-//               written back over S in TMEM as bf16 pairs and PV reads it
+//               row = TMEM lane): S from TMEM (on unmasked tiles with the
+//               reducing load of sm_103a, which also returns the row max),
+//               mask, row max, exp2; P is written to TMEM as bf16 pairs (over
+//               S at D = 128, into its own columns at D = 64) and PV reads it
 //               from there (the A operand of tcgen05.mma may live in TMEM).
 //               On the partial tiles of the first query tile of each stream P
 //               is also split into hi + lo bf16 terms (two PV passes): the rows
